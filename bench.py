@@ -1,0 +1,513 @@
+"""Benchmark of the Lizard-attention operator on GB300.
+
+One step = lizard_attn_fwd + lizard_attn_bwd over the Llama-3-8B attention-layer
+workload (B=1, H=32, L=4096, d=128, W=64, M=4, bf16 tensors, fp32 log-gate/state).
+``value`` is tokens/s of the whole job (B*L tokens per step per GPU, all heads); every
+rank runs its own independent batch (weak scaling, no collective on the data path).
+
+Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the launch
+stream with an L2 flush (a 256 MiB write) between steps, outside the events; inputs are
+also larger than L2.  A barrier and a device synchronise bracket the timed region and
+the slowest rank's time is reported.  ``e2e`` repeats the step through the same public
+calls with pinned host buffers, copying inputs in and every output back each step.
+``--impl reference`` times the fp64 oracle on the host cores on a bounded sample of the
+same workload and prints the same kind of line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Lizard-attn fwd/bwd tokens/sec (L=4096,H=32,d=128,bf16); % roofline"
+WORKLOAD = "llama3_8b_fwd"  # shapes of the metric's configuration
+NAMES = ("phi_q", "phi_k", "v", "log_gamma", "q", "k", "meta_k", "meta_v")
+
+# Algorithmic HBM bytes per (token, head) of each kernel at d = 128 (bf16 tensors, fp32
+# log gamma): what the kernel must read and write at minimum.
+ALGO_BYTES_PER_TOKEN_HEAD = {
+    "fwd_simt": 5 * 256 + 512 + 256,          # phi_q, phi_k, v, q, k + log_gamma + y
+    "gla_bwd_simt": 4 * 256 + 512 + 2 * 256 + 512,  # phi_q, phi_k, v, dy, lg; d_phi_q/k, d_lg
+    "win_bwd_query": 4 * 256 + 256,           # q, k, v, dy + d_q
+    "win_bwd_key": 4 * 256 + 2 * 256,         # q, k, v, dy + d_k, d_v
+}
+DECODE_BYTES_PER_UNIT = 2 * 65536 + 2 * 64 * 128 * 2 + 5 * 256 + 512 + 2 * 256 + 256
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _workload_dims():
+    import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    return w
+
+
+# --------------------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# --------------------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    import synth
+
+    w = _workload_dims()
+    cores = os.cpu_count() or 1
+    heads = max(1, min(cores, 16, w["H"]))
+    # Bounded sample: `heads` of the 32 heads of the workload, full length, fwd + bwd.
+    x = synth.make_fwd_inputs(1, heads, w["L"], w["dk"], w["dv"], w["M"], "bf16", w["gate"],
+                              seed=w["seed"], with_dy=True)
+    oracle.build()
+
+    def step():
+        oracle.fwd(*(x[n] for n in NAMES), W=w["W"], nthreads=heads)
+        oracle.bwd(*(x[n] for n in NAMES), x["dy"], W=w["W"], nthreads=heads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    tokens_equiv = w["L"] * heads / w["H"]  # one token = all H heads
+    value = tokens_equiv / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.last_threads(),
+                         "kind": "oracle",
+                         "sample": f"fwd+bwd of {heads} of {w['H']} heads, L={w['L']}, "
+                                   f"d={w['dk']} (fp64 C oracle, one thread per head)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(w):
+    return {"workload": f"Llama-3-8B attention layer fwd+bwd: B={w['B']}, H={w['H']}, "
+                        f"L={w['L']}, dk=dv={w['dk']}, W={w['W']}, M={w['M']}, alpha=1",
+            "B": w["B"], "H": w["H"], "L": w["L"], "d": w["dk"], "W": w["W"], "M": w["M"],
+            "step": "lizard_attn_fwd + lizard_attn_bwd",
+            "l2": "inputs larger than L2; 256 MiB L2 flush between timed steps"}
+
+
+# --------------------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------------------
+class Problem:
+    """Device tensors of one fwd+bwd step (inputs resident in HBM)."""
+
+    def __init__(self, x, w, dev):
+        import torch
+
+        import hybrid_gated_linear_gb300 as lz
+        self.lz = lz
+        self.w = w
+        B, H, L, d, M = w["B"], w["H"], w["L"], w["dk"], w["M"]
+        bf = torch.bfloat16
+        self.t = {}
+        for n, a in x.items():
+            t = torch.from_numpy(a).to(dev)
+            self.t[n] = t if n == "log_gamma" else t.to(bf)
+        self.dims = lz.lizard_dims(B, H, L, d, d, M, lz.LIZARD_BF16, 0.0)
+        self.y = torch.empty(B, H, L, d, dtype=bf, device=dev)
+        self.g = {n: torch.empty(B, H, L, d, dtype=bf, device=dev)
+                  for n in ("d_phi_q", "d_phi_k", "d_v", "d_q", "d_k")}
+        self.g["d_log_gamma"] = torch.empty(B, H, L, d, dtype=torch.float32, device=dev)
+        self.g["d_meta_k"] = torch.empty(H, M, d, dtype=torch.float32, device=dev)
+        self.g["d_meta_v"] = torch.empty(H, M, d, dtype=torch.float32, device=dev)
+        self.ws_f = torch.zeros(max(16, lz.lizard_fwd_workspace_bytes(self.dims, w["W"])),
+                                dtype=torch.uint8, device=dev)
+        self.ws_b = torch.zeros(lz.lizard_bwd_workspace_bytes(self.dims, w["W"]),
+                                dtype=torch.uint8, device=dev)
+        self.launches = 0
+
+    def fwd(self, stream=None):
+        lz, t = self.lz, self.t
+        lz.lizard_attn_fwd(self.dims, *(t[n] for n in NAMES), self.w["W"], 1.0, self.y, None,
+                           None, self.ws_f, stream)
+        self.launches += lz.lizard_last_launch_count()
+
+    def bwd(self, stream=None):
+        lz, t, g = self.lz, self.t, self.g
+        lz.lizard_attn_bwd(self.dims, *(t[n] for n in NAMES), self.w["W"], 1.0, None, t["dy"],
+                           g["d_phi_q"], g["d_phi_k"], g["d_v"], g["d_log_gamma"], g["d_q"],
+                           g["d_k"], g["d_meta_k"], g["d_meta_v"], None, self.ws_b, stream)
+        self.launches += lz.lizard_last_launch_count()
+
+    def step(self, stream=None):
+        self.fwd(stream)
+        self.bwd(stream)
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, world, dev):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _time_steps(fn, steps, flush, stream):
+    import torch
+    times = []
+    for _ in range(steps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in times]
+
+
+def _roofline_from_trace(trace, w, peaks, steps):
+    """Dominant kernel over the timed steps -> roofline object."""
+    tot, cnt = {}, {}
+    for name, ms in trace:
+        tot[name] = tot.get(name, 0.0) + ms
+        cnt[name] = cnt.get(name, 0) + 1
+    if not tot:
+        return None, {}
+    dom = max(tot, key=tot.get)
+    units = w["B"] * w["H"] * w["L"]
+    per_launch_ms = tot[dom] / cnt[dom]
+    algo = ALGO_BYTES_PER_TOKEN_HEAD.get(dom)
+    kernels = {k: {"launches_per_step": cnt[k] / steps, "ms_per_launch": tot[k] / cnt[k],
+                   "share": tot[k] / sum(tot.values())} for k in tot}
+    if algo is None:
+        return {"kernel": dom, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": None, "traffic": None}, kernels
+    achieved = algo * units / (per_launch_ms * 1e-3) / 1e9
+    return {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+            "algorithmic_bytes_per_launch": algo * units,
+            "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"}, kernels
+
+
+def _decode_part(dev, stream, peaks, steps=64):
+    """Decode workload (64 sequences x 32 heads, W=64, M=4): a CUDA graph of `steps`
+    decode calls, timed with events; returns per-step numbers."""
+    import torch
+
+    import hybrid_gated_linear_gb300 as lz
+    import synth
+    w = synth.WORKLOADS["decode_64x32"]
+    s = synth.decode_stream("decode_64x32")
+    bf = torch.bfloat16
+    dims = lz.lizard_decode_dims(w["N"], w["H"], w["dk"], w["dv"], w["M"], lz.LIZARD_BF16, 0.0)
+    h = torch.from_numpy(s.h0).to(dev)
+    kr = torch.from_numpy(s.k_ring).to(dev).to(bf)
+    vr = torch.from_numpy(s.v_ring).to(dev).to(bf)
+    pos = torch.from_numpy(s.pos0).to(dev)
+    mk = torch.from_numpy(s.meta_k).to(dev).to(bf)
+    mv = torch.from_numpy(s.meta_v).to(dev).to(bf)
+    ws = torch.zeros(lz.lizard_decode_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+    y = torch.empty(w["N"], w["H"], w["dv"], dtype=bf, device=dev)
+    toks = []
+    for _ in range(8):
+        tk = s.next_token()
+        d = {n: torch.from_numpy(a).to(dev) for n, a in tk.items()}
+        for n in ("phi_q", "phi_k", "v", "q", "k"):
+            d[n] = d[n].to(bf)
+        toks.append(d)
+
+    def one(i):
+        d = toks[i % len(toks)]
+        lz.lizard_decode_step(dims, d["phi_q"], d["phi_k"], d["v"], d["log_gamma"], d["q"],
+                              d["k"], mk, mv, w["W"], 1.0, h, kr, vr, pos, y, ws,
+                              torch.cuda.current_stream())
+
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for i in range(3):
+            one(i)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(steps):
+            one(i)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    reps = 5
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / (reps * steps)
+    units = w["N"] * w["H"]
+    gbs = DECODE_BYTES_PER_UNIT * units / (us * 1e-6) / 1e9
+    return {"workload": "decode: 64 sequences x 32 heads, d=128, W=64, M=4 (CUDA graph of "
+                        f"{steps} steps)", "us_per_step": us,
+            "tokens_per_s": w["N"] / (us * 1e-6),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "algorithmic_bytes_per_step": DECODE_BYTES_PER_UNIT * units}}
+
+
+def _e2e(prob, x, steps, dev):
+    """Same step through the public calls with pinned host buffers: H2D copy of every
+    input, fwd + bwd, D2H copy of y and every gradient, each step."""
+    import torch
+    host_in = {n: torch.from_numpy(a).to(prob.t[n].dtype).pin_memory() for n, a in x.items()}
+    outs = [prob.y] + list(prob.g.values())
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for n, t in host_in.items():
+            prob.t[n].copy_(t, non_blocking=True)
+        prob.step()
+        for o, hbuf in zip(outs, host_out):
+            hbuf.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def _cpu_baseline(w, budget_s=20.0):
+    import oracle
+    import synth
+    cores = os.cpu_count() or 1
+    heads = max(1, min(cores, 16, w["H"]))
+    x = synth.make_fwd_inputs(1, heads, w["L"], w["dk"], w["dv"], w["M"], "bf16", w["gate"],
+                              seed=w["seed"], with_dy=True)
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.fwd(*(x[n] for n in NAMES), W=w["W"], nthreads=heads)
+    oracle.bwd(*(x[n] for n in NAMES), x["dy"], W=w["W"], nthreads=heads)
+    dt = time.perf_counter() - t0
+    return {"value": w["L"] * heads / w["H"] / dt, "unit": "tokens/s",
+            "cores": oracle.last_threads(), "kind": "oracle",
+            "sample": f"one fwd+bwd of {heads} of {w['H']} heads at L={w['L']}, d={w['dk']} "
+                      f"({dt:.1f} s wall, fp64 C oracle, one thread per head)"}
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import hybrid_gated_linear_gb300 as lz
+    import synth
+    lz.build()
+    lz.library()
+    w = _workload_dims()
+    peaks = _peaks()
+    x = synth.make_fwd_inputs(w["B"], w["H"], w["L"], w["dk"], w["dv"], w["M"], "bf16",
+                              w["gate"], seed=w["seed"] + rank, with_dy=True)
+    prob = Problem(x, w, dev)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def flush():
+        flush_buf.fill_(1)
+
+    for _ in range(args.warmup):
+        prob.step()
+    torch.cuda.synchronize()
+
+    with ClockSampler(local) as clk:
+        _barrier(world)
+        torch.cuda.synchronize()
+        prob.launches = 0
+        lz.lizard_trace_enable(True)
+        times = _time_steps(prob.step, args.steps, flush, stream)
+        lz.lizard_trace_enable(False)
+        trace = lz.lizard_trace_read()
+        torch.cuda.synchronize()
+        _barrier(world)
+        launches = prob.launches
+        # fwd-only timing (same hygiene) for the per-pass breakdown
+        fwd_times = _time_steps(prob.fwd, args.steps, flush, stream)
+        bwd_times = _time_steps(prob.bwd, args.steps, flush, stream)
+    clocks = clk.summary()
+
+    ms = statistics.mean(times)
+    ms = _max_over_ranks(ms, world, dev)
+    tokens = w["B"] * w["L"]
+    value = world * tokens / (ms * 1e-3)
+    roof, kernels = _roofline_from_trace(trace, w, peaks, args.steps)
+    fwd_ms = statistics.mean(fwd_times)
+    bwd_ms = statistics.mean(bwd_times)
+    units = w["B"] * w["H"] * w["L"]
+    fwd_bytes = 2048 * units
+    bwd_bytes = 3840 * units
+    parts = {
+        "fwd": {"ms": fwd_ms, "tokens_per_s": tokens / (fwd_ms * 1e-3),
+                "roofline_frac": fwd_bytes / (fwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "algorithmic_bytes": fwd_bytes},
+        "bwd": {"ms": bwd_ms, "tokens_per_s": tokens / (bwd_ms * 1e-3),
+                "roofline_frac": bwd_bytes / (bwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "algorithmic_bytes": bwd_bytes},
+        "kernels": kernels,
+    }
+    try:
+        parts["decode"] = _decode_part(dev, stream, peaks)
+    except Exception as e:  # reported, never hidden
+        parts["decode"] = {"error": repr(e)}
+    e2e_ms, h2d, d2h = _e2e(prob, x, max(3, args.steps // 2), dev)
+    e2e_ms = _max_over_ranks(e2e_ms, world, dev)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian inputs, random meta tokens)",
+        "config": _config(w), "roofline": roof, "gpu_launches": launches, "clocks": clocks,
+        "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "parts": parts,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = _cpu_baseline(w)
+        except Exception as e:
+            line["cpu_baseline"] = {"error": repr(e)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

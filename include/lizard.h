@@ -1,0 +1,189 @@
+/*
+ * lizard.h -- C ABI of the GB300 (sm_103a) Lizard-attention library.
+ *
+ * The operator (sources cited per call below):
+ *   GLA branch     h_i = gamma_i (.) h_{i-1} + phi_k_i v_i^T,   y_gla_i = phi_q_i^T h_i
+ *                  with gamma_i = exp(log_gamma_i) per key dimension, scaling the rows of
+ *                  h (the key dimension).  ["Lizard: An Efficient Linearization Framework
+ *                  for Large Language Models", papernotes.org note, 方法详解/关键设计:
+ *                  GLA replacing RoPE; arXiv 2507.09025, Method: parallel GLA form]
+ *   Window branch  y_win_i = softmax(scale * [q_i.meta_k ; q_i.k_j]) [meta_v ; v_j] over the
+ *                  M meta tokens and the W tokens j in [max(0, i-W+1), i].
+ *                  [papernotes.org note, 关键设计: Anchor Window Attention]
+ *   Merge          y = y_gla + alpha * y_win.  [papernotes.org note, 整体框架]
+ *
+ * Conventions shared by every call:
+ *   - Device pointers only (unless stated), caller-owned; the library never allocates,
+ *     frees or keeps a pointer after the call returns.  Buffers must stay alive until the
+ *     work queued on `stream` has finished.
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy default stream.
+ *     Every call is asynchronous: it validates arguments on the host, enqueues kernels
+ *     and returns; only lizard_check_device_errors synchronises.
+ *   - Per-token tensors are contiguous row-major [B,H,L,d] ("BHLD"); meta tensors are
+ *     [H,M,d] (one set per head, shared by every batch entry); states are [B,H,dk,dv]
+ *     fp32 with dk the row (gated) dimension.
+ *   - "T" tensors (phi_q, phi_k, v, q, k, meta_k, meta_v, y, dy, d_phi_q, d_phi_k, d_v,
+ *     d_q, d_k) have the element type `dtype` (fp32 or bf16); log_gamma, states and
+ *     d_log_gamma, d_meta_* are always fp32.  Accumulation is fp32 throughout.
+ *   - The raw q/k of the window branch have dimension dk (same as phi_q/phi_k).
+ *   - Every pointer must be 16-byte aligned.  Outputs must not alias inputs (the decode
+ *     state h, rings and pos are in-out by design).
+ *   - Errors: invalid arguments return a status before anything is enqueued; a failed
+ *     launch returns LIZARD_ERR_CUDA; conditions found on the device (a bounded wait that
+ *     ran out, a range guard) set a word in the workspace that
+ *     lizard_check_device_errors reads.  Nothing throws across this boundary.
+ */
+#ifndef LIZARD_H
+#define LIZARD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LIZARD_ABI_VERSION 1
+
+typedef enum lizard_status {
+    LIZARD_OK = 0,
+    LIZARD_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, aliasing */
+    LIZARD_ERR_UNSUPPORTED = 2,   /* valid but not built (e.g. head dim not 64/128) */
+    LIZARD_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    LIZARD_ERR_TIMEOUT = 4,       /* a device-side bounded wait ran out (device word) */
+    LIZARD_ERR_DEVICE_CHECK = 5,  /* a device-side guard fired (device word) */
+    LIZARD_ERR_WORKSPACE = 6      /* workspace missing or smaller than required */
+} lizard_status;
+
+typedef enum lizard_dtype { LIZARD_F32 = 0, LIZARD_BF16 = 1 } lizard_dtype;
+
+/* Shape of a forward/backward call. */
+typedef struct lizard_dims {
+    int32_t B;            /* batch, >= 1 */
+    int32_t H;            /* heads, >= 1 */
+    int32_t L;            /* tokens, >= 0 (0 is a no-op apart from h_final) */
+    int32_t dk;           /* key/query dim: 64 or 128 */
+    int32_t dv;           /* value dim: equal to dk */
+    int32_t M;            /* meta tokens per head, 0..16 */
+    lizard_dtype dtype;   /* element type of the "T" tensors */
+    float scale;          /* window softmax scale; <= 0 selects 1/sqrt(dk) */
+} lizard_dims;
+
+/* Shape of one decode step: N sequences, one new token each. */
+typedef struct lizard_decode_dims {
+    int32_t N, H, dk, dv, M;
+    lizard_dtype dtype;
+    float scale;
+} lizard_decode_dims;
+
+/* Device-workspace bytes each call needs (0 means workspace may be NULL). */
+size_t lizard_fwd_workspace_bytes(const lizard_dims* dims, int32_t W);
+size_t lizard_bwd_workspace_bytes(const lizard_dims* dims, int32_t W);
+size_t lizard_decode_workspace_bytes(const lizard_decode_dims* dims);
+
+/*
+ * Forward pass: y = y_gla + alpha * y_win.
+ *   phi_q, phi_k, q, k [B,H,L,dk] T;  v [B,H,L,dv] T;  log_gamma [B,H,L,dk] fp32 (<= 0
+ *   expected; any finite value is accepted);  meta_k [H,M,dk], meta_v [H,M,dv] T (NULL
+ *   when M = 0);  W >= 1 window length (keys including self; the backward needs
+ *   min(W, L) <= 4096, else LIZARD_ERR_UNSUPPORTED);  alpha any finite value.
+ *   y [B,H,L,dv] T output.  h0 [B,H,dk,dv] fp32 initial state or NULL (zeros).
+ *   h_final [B,H,dk,dv] fp32 final state or NULL.
+ * The GLA branch is computed chunkwise with the decay products absorbed in log space
+ * into the query/key features ("Lizard", arXiv 2507.09025, Method: hardware-aware
+ * reparameterisation); the result equals the recurrence up to rounding.
+ */
+lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* phi_q, const void* phi_k,
+                              const void* v, const float* log_gamma, const void* q,
+                              const void* k, const void* meta_k, const void* meta_v,
+                              int32_t W, float alpha, void* y, const float* h0,
+                              float* h_final, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
+ * Backward pass of lizard_attn_fwd for the loss sum(y * dy).
+ *   Inputs as in lizard_attn_fwd plus dy [B,H,L,dv] T.
+ *   Outputs: d_phi_q, d_phi_k, d_q, d_k [B,H,L,dk] T; d_v [B,H,L,dv] T (GLA + window);
+ *   d_log_gamma [B,H,L,dk] fp32; d_meta_k [H,M,dk], d_meta_v [H,M,dv] fp32, summed over
+ *   batch and tokens (NULL when M = 0); d_h0 [B,H,dk,dv] fp32 or NULL.
+ * The pages give no backward formulas; this is the exact adjoint of the forward.  The
+ * log-gate gradient uses d log_gamma_t = sum_{t'>=t} (phi_q (.) d_phi_q - phi_k (.) d_phi_k)_{t'}
+ * (exact because the gate enters only through its cumulative sums).  Deterministic:
+ * no floating-point atomics.
+ */
+lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* phi_q, const void* phi_k,
+                              const void* v, const float* log_gamma, const void* q,
+                              const void* k, const void* meta_k, const void* meta_v,
+                              int32_t W, float alpha, const float* h0, const void* dy,
+                              void* d_phi_q, void* d_phi_k, void* d_v, float* d_log_gamma,
+                              void* d_q, void* d_k, float* d_meta_k, float* d_meta_v,
+                              float* d_h0, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
+ * One recurrent decode step for N sequences (constant memory per sequence: the state
+ * and a W-slot ring; "Lizard", arXiv 2507.09025, Preliminaries: recurrent form).
+ *   Token inputs phi_q, phi_k, q, k [N,H,dk] T; v [N,H,dv] T; log_gamma [N,H,dk] fp32.
+ *   meta_k [H,M,dk], meta_v [H,M,dv] T.  W >= 1 ring length (= window length).
+ *   In-out: h [N,H,dk,dv] fp32; k_ring [N,H,W,dk] T; v_ring [N,H,W,dv] T; pos [N] int64
+ *   (device) = absolute position of the new token, >= 0.
+ *   Per sequence n at position p = pos[n]: h <- gamma (.) h + phi_k v^T; y_gla = phi_q^T h;
+ *   ring slot p mod W <- (k, v); y_win = softmax over the M meta tokens and the
+ *   min(p+1, W) tokens [max(0, p-W+1), p]; y = y_gla + alpha * y_win; pos[n] <- p + 1.
+ *   y [N,H,dv] T output.
+ * Workspace: lizard_decode_workspace_bytes(dims) bytes that must be zero-filled before
+ * the first step (lizard_workspace_init does that); each step leaves it zeroed again.
+ * A workspace must not be shared by steps that run concurrently.
+ */
+lizard_status lizard_decode_step(const lizard_decode_dims* dims, const void* phi_q,
+                                 const void* phi_k, const void* v, const float* log_gamma,
+                                 const void* q, const void* k, const void* meta_k,
+                                 const void* meta_v, int32_t W, float alpha, float* h,
+                                 void* k_ring, void* v_ring, int64_t* pos, void* y,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Chunk-local inclusive cumulative sum of log gamma (the reference point of the
+ * log-space reparameterisation; "Lizard", arXiv 2507.09025, Method: cumulative gate
+ * products c_t).  log_gamma [units,L,dk] fp32 -> b [units,L,dk] fp32 with
+ * b_t = sum_{s = chunk start..t} log_gamma_s, chunks [c*chunk, min((c+1)*chunk, L));
+ * gamma_chunk [units, ceil(L/chunk), dk] fp32 = b at each chunk's last token (nullable).
+ * dk in 1..1024, chunk in 1..1024.
+ */
+lizard_status lizard_chunk_cumsum(int32_t units, int32_t L, int32_t dk, int32_t chunk,
+                                  const float* log_gamma, float* b, float* gamma_chunk,
+                                  void* stream);
+
+/* Zero-fills a workspace on `stream` (asynchronous). */
+lizard_status lizard_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word in `workspace`.
+ * Returns LIZARD_OK, LIZARD_ERR_TIMEOUT or LIZARD_ERR_DEVICE_CHECK (or LIZARD_ERR_CUDA if
+ * the stream itself reports an error).
+ */
+lizard_status lizard_check_device_errors(void* workspace, void* stream);
+
+/* Static description of a status code. */
+const char* lizard_status_string(lizard_status status);
+
+/* LIZARD_ABI_VERSION of the library that was loaded. */
+int32_t lizard_abi_version(void);
+
+/* Number of kernels the most recent call of this thread enqueued (for launch counts). */
+int32_t lizard_last_launch_count(void);
+
+/*
+ * Per-kernel device timing.  While enabled (per host thread), every kernel the library
+ * enqueues is bracketed by two CUDA events on its stream.  lizard_trace_read waits for
+ * the recorded events, writes up to max_records NUL-terminated kernel names (name_len
+ * bytes each) and durations in milliseconds, returns the count and clears the log.
+ */
+lizard_status lizard_trace_enable(int32_t enable);
+int32_t lizard_trace_read(char* names, int32_t name_len, float* ms, int32_t max_records);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIZARD_H */

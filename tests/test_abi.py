@@ -1,0 +1,167 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads, it
+exports every function ``include/lizard.h`` declares, and argument validation returns
+the documented status before anything is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import hybrid_gated_linear_gb300 as lz
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lizard.h")
+
+OK, INVALID, UNSUPPORTED, CUDA, TIMEOUT, CHECK, WORKSPACE = range(7)
+A = 0x7f0000000000  # fake, 16-byte aligned device addresses: validation never dereferences
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lz.build()
+    return lz.library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lizard_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert sorted(lz.EXPORTED_SYMBOLS) == _declared_functions()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_abi_version(lib):
+    m = re.search(r"#define LIZARD_ABI_VERSION (\d+)", open(HEADER).read())
+    assert lib.lizard_abi_version() == int(m.group(1))
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lib.lizard_status_string(s)
+    assert lz.lizard_status_string(OK) == "ok"
+
+
+def _dims(**kw):
+    d = dict(B=1, H=2, L=64, dk=128, dv=128, M=4, dtype=lz.LIZARD_BF16, scale=0.0)
+    d.update(kw)
+    return lz.lizard_dims(**d)
+
+
+def _fwd(lib, dims, W=64, alpha=1.0, ptrs=None, ws=A + 0x100000, ws_bytes=1 << 20, meta=True):
+    p = [ctypes.c_void_p(A + i * 0x1000000) for i in range(6)] if ptrs is None else ptrs
+    mk = ctypes.c_void_p(A + 0x20000000) if meta else None
+    mv = ctypes.c_void_p(A + 0x21000000) if meta else None
+    y = ctypes.c_void_p(A + 0x30000000)
+    return lib.lizard_attn_fwd(ctypes.byref(dims) if dims is not None else None, *p, mk, mv, W,
+                               alpha, y, None, None, ctypes.c_void_p(ws) if ws else None,
+                               ws_bytes, None)
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    assert _fwd(lib, None) == INVALID
+    assert _fwd(lib, _dims(), W=0) == INVALID
+    assert _fwd(lib, _dims(B=0)) == INVALID
+    assert _fwd(lib, _dims(M=17)) == INVALID
+    assert _fwd(lib, _dims(M=-1)) == INVALID
+    assert _fwd(lib, _dims(dtype=7)) == INVALID
+    assert _fwd(lib, _dims(L=-3)) == INVALID
+    assert _fwd(lib, _dims(), alpha=float("nan")) == INVALID
+    assert _fwd(lib, _dims(M=2), meta=False) == INVALID
+    bad = [ctypes.c_void_p(A + i * 0x1000000) for i in range(6)]
+    bad[2] = ctypes.c_void_p(A + 8)  # misaligned v
+    assert _fwd(lib, _dims(), ptrs=bad) == INVALID
+    null = list(bad)
+    null[2] = None
+    assert _fwd(lib, _dims(), ptrs=null) == INVALID
+
+
+def test_fwd_unsupported_shapes(lib):
+    assert _fwd(lib, _dims(dk=96, dv=96)) == UNSUPPORTED
+    assert _fwd(lib, _dims(dk=128, dv=64)) == UNSUPPORTED
+
+
+def test_fwd_workspace_checks(lib):
+    need = lib.lizard_fwd_workspace_bytes(ctypes.byref(_dims()), 64)
+    assert need >= 4
+    assert _fwd(lib, _dims(), ws=None, ws_bytes=0) == WORKSPACE
+    assert _fwd(lib, _dims(), ws_bytes=need - 1) == WORKSPACE
+
+
+def test_fwd_rejects_output_aliasing_an_input(lib):
+    p = [ctypes.c_void_p(A + i * 0x1000000) for i in range(6)]
+    dims = _dims()
+    y = p[0]  # y == phi_q
+    st = lib.lizard_attn_fwd(ctypes.byref(dims), *p, ctypes.c_void_p(A + 0x20000000),
+                             ctypes.c_void_p(A + 0x21000000), 64, 1.0, y, None, None,
+                             ctypes.c_void_p(A + 0x40000000), 1 << 20, None)
+    assert st == INVALID
+
+
+def test_bwd_workspace_grows_with_problem(lib):
+    small = lib.lizard_bwd_workspace_bytes(ctypes.byref(_dims(L=64)), 64)
+    big = lib.lizard_bwd_workspace_bytes(ctypes.byref(_dims(L=4096, B=2)), 64)
+    assert 0 < small < big
+    assert lib.lizard_bwd_workspace_bytes(ctypes.byref(_dims(dk=96, dv=96)), 64) == 0
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    dims = _dims()
+    P = lambda i: ctypes.c_void_p(A + i * 0x1000000)
+    args = [P(i) for i in range(8)]
+    grads = [P(20 + i) for i in range(8)]
+    ws = P(40)
+    need = lib.lizard_bwd_workspace_bytes(ctypes.byref(dims), 64)
+    st = lib.lizard_attn_bwd(ctypes.byref(dims), *args, 64, 1.0, None, P(10), *grads, None, ws,
+                             need - 1, None)
+    assert st == WORKSPACE
+    grads2 = list(grads)
+    grads2[1] = grads2[0]  # two outputs alias
+    st = lib.lizard_attn_bwd(ctypes.byref(dims), *args, 64, 1.0, None, P(10), *grads2, None, ws,
+                             need, None)
+    assert st == INVALID
+
+
+def test_decode_rejects_bad_arguments(lib):
+    d = lz.lizard_decode_dims(4, 2, 128, 128, 4, lz.LIZARD_BF16, 0.0)
+    P = lambda i: ctypes.c_void_p(A + i * 0x1000000)
+    base = [P(i) for i in range(8)]
+    need = lib.lizard_decode_workspace_bytes(ctypes.byref(d))
+    assert need > 0
+
+    def call(W=64, ws_bytes=need, dims=d, extra=None):
+        outs = [P(20 + i) for i in range(5)] if extra is None else extra
+        return lib.lizard_decode_step(ctypes.byref(dims), *base, W, 1.0, *outs, P(40), ws_bytes,
+                                      None)
+
+    assert call(W=0) == INVALID
+    assert call(W=4096) == INVALID
+    assert call(ws_bytes=need - 1) == WORKSPACE
+    outs = [P(20 + i) for i in range(5)]
+    outs[4] = base[0]  # y aliases phi_q
+    assert call(extra=outs) == INVALID
+    d2 = lz.lizard_decode_dims(4, 2, 80, 80, 4, lz.LIZARD_BF16, 0.0)
+    assert call(dims=d2) == UNSUPPORTED
+
+
+def test_chunk_cumsum_rejects_bad_arguments(lib):
+    P = lambda i: ctypes.c_void_p(A + i * 0x1000000)
+    assert lib.lizard_chunk_cumsum(0, 10, 4, 64, P(0), P(1), None, None) == INVALID
+    assert lib.lizard_chunk_cumsum(1, 10, 4, 0, P(0), P(1), None, None) == INVALID
+    assert lib.lizard_chunk_cumsum(1, 10, 4, 64, P(0), P(0), None, None) == INVALID
+    assert lib.lizard_chunk_cumsum(1, 10, 4, 64, P(0), None, None, None) == INVALID
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import importlib
+    monkeypatch.setattr(lz, "_lib", None)
+    monkeypatch.setattr(lz, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        lz.library()
+    importlib.reload(lz)
