@@ -81,7 +81,7 @@ static int run_units(long n, int nthreads, unit_fn fn, void *ctx) {
     pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)t);
     int started = 0;
     if (th) {
-        for (int i = 0; i < t; ++i) {
+        for (int i = 0; i < t - 1; ++i) { /* the calling thread is the t-th worker */
             if (pthread_create(&th[started], NULL, unit_worker, &p) == 0) ++started;
         }
     }
