@@ -22,17 +22,20 @@ __all__ = [
     "lizard_fwd_workspace_bytes", "lizard_bwd_workspace_bytes", "lizard_decode_workspace_bytes",
     "lizard_workspace_init", "lizard_check_device_errors", "lizard_status_string",
     "lizard_abi_version", "lizard_last_launch_count", "lizard_trace_enable", "lizard_trace_read",
+    "lizard_decode_step_noalloc", "LIZARD_NOALLOC_MAX_SEQUENCES",
     "LIZARD_F32", "LIZARD_BF16", "EXPORTED_SYMBOLS",
 ]
 
 LIZARD_F32 = 0
 LIZARD_BF16 = 1
+LIZARD_NOALLOC_MAX_SEQUENCES = 16384
 
 EXPORTED_SYMBOLS = (
     "lizard_attn_fwd", "lizard_attn_bwd", "lizard_decode_step", "lizard_chunk_cumsum",
     "lizard_fwd_workspace_bytes", "lizard_bwd_workspace_bytes", "lizard_decode_workspace_bytes",
     "lizard_workspace_init", "lizard_check_device_errors", "lizard_status_string",
     "lizard_abi_version", "lizard_last_launch_count", "lizard_trace_enable", "lizard_trace_read",
+    "lizard_decode_step_noalloc",
 )
 
 STATUS_NAMES = {0: "LIZARD_OK", 1: "LIZARD_ERR_INVALID_ARG", 2: "LIZARD_ERR_UNSUPPORTED",
@@ -94,6 +97,7 @@ def library():
                 "lizard_last_launch_count": (I32, []),
                 "lizard_trace_enable": (I32, [I32]),
                 "lizard_trace_read": (I32, [ctypes.c_char_p, I32, ctypes.POINTER(F), I32]),
+                "lizard_decode_step_noalloc": (I32, [DDP] + [P] * 8 + [I32, F] + [P] * 5 + [P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -237,3 +241,17 @@ def lizard_trace_read(max_records: int = 4096):
     raw = names.raw
     return [(raw[i * name_len:(i + 1) * name_len].split(b"\0", 1)[0].decode(), float(ms[i]))
             for i in range(n)]
+
+
+def lizard_decode_step_noalloc(dims: lizard_decode_dims, phi_q, phi_k, v, log_gamma, q, k,
+                               meta_k, meta_v, W: int, alpha: float, h, k_ring, v_ring, pos, y,
+                               stream=None):
+    """lizard_decode_step without a workspace, for callers that cannot allocate device
+    memory: the library's own fixed device array holds the per-sequence counters (N at
+    most LIZARD_NOALLOC_MAX_SEQUENCES).  Calls that overlap on the GPU race on that array."""
+    st = library().lizard_decode_step_noalloc(ctypes.byref(dims), _ptr(phi_q), _ptr(phi_k),
+                                              _ptr(v), _ptr(log_gamma), _ptr(q), _ptr(k),
+                                              _ptr(meta_k), _ptr(meta_v), int(W), float(alpha),
+                                              _ptr(h), _ptr(k_ring), _ptr(v_ring), _ptr(pos),
+                                              _ptr(y), _stream(stream))
+    _check(st, "lizard_decode_step_noalloc")

@@ -143,6 +143,30 @@ lizard_status lizard_decode_step(const lizard_decode_dims* dims, const void* phi
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Allocation-free decode step (the paper has no counterpart; this is a library service).
+ * For callers that cannot allocate device memory: a host program or language binding
+ * that embeds this library without a device allocator of its own, or a serving runtime
+ * whose memory pool owns all device memory and may not call cudaMalloc on the per-token
+ * path.  Same arguments and results as lizard_decode_step, without the workspace: the
+ * per-sequence counters live in a fixed device array inside the library (a little over
+ * 64 KiB, held on every GPU that uses it until the process exits), so N is limited to
+ * LIZARD_NOALLOC_MAX_SEQUENCES; a larger N returns LIZARD_ERR_UNSUPPORTED before anything
+ * is enqueued.  The first call on each device looks up the array's address on the
+ * current device; make that first call before any stream capture begins.  Each call
+ * clears the counters on `stream` before its kernel.  Every call in the process shares
+ * the one array, so calls whose work overlaps on the GPU (other streams, other threads)
+ * race on it: order them.  These calls report no device status word and are not counted
+ * by lizard_last_launch_count.  Nothing is allocated or freed.
+ */
+#define LIZARD_NOALLOC_MAX_SEQUENCES 16384
+lizard_status lizard_decode_step_noalloc(const lizard_decode_dims* dims, const void* phi_q,
+                                         const void* phi_k, const void* v,
+                                         const float* log_gamma, const void* q, const void* k,
+                                         const void* meta_k, const void* meta_v, int32_t W,
+                                         float alpha, float* h, void* k_ring, void* v_ring,
+                                         int64_t* pos, void* y, void* stream);
+
+/*
  * Chunk-local inclusive cumulative sum of log gamma (the reference point of the
  * log-space reparameterisation; "Lizard", arXiv 2507.09025, Method: cumulative gate
  * products c_t).  log_gamma [units,L,dk] fp32 -> b [units,L,dk] fp32 with
