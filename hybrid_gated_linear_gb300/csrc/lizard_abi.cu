@@ -168,7 +168,8 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* phi_q, const 
                 phi_q, phi_k, v, log_gamma, q, k, meta_k, meta_v, y, h0, h_final,
                 static_cast<unsigned*>(workspace)};
   int launches = 0;
-  e = lz::launch_fwd_simt(a, d.dtype, s, &launches);
+  e = lz::fwd_tc_supported(a, d.dtype) ? lz::launch_fwd_tc(a, s, &launches)
+                                       : lz::launch_fwd_simt(a, d.dtype, s, &launches);
   g_last_launches = launches;
   return cuda_status(e);
 }

@@ -70,6 +70,9 @@ void trace_end(cudaStream_t s);
 cudaError_t launch_chunk_cumsum(int units, int L, int dk, int chunk, const float* lg, float* b,
                                 float* gamma_chunk, cudaStream_t s, int* launches);
 cudaError_t launch_fwd_simt(const FwdArgs& a, lizard_dtype dt, cudaStream_t s, int* launches);
+// Tensor-core forward (bf16, dk = dv = 128, W <= 129, M <= 16).
+bool fwd_tc_supported(const FwdArgs& a, lizard_dtype dt);
+cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s, int* launches);
 size_t bwd_simt_workspace(int B, int H, int L, int dk, int dv, int M);
 cudaError_t launch_bwd_simt(const BwdArgs& a, lizard_dtype dt, cudaStream_t s, int* launches);
 cudaError_t launch_decode(const DecArgs& a, lizard_dtype dt, cudaStream_t s, int* launches);
