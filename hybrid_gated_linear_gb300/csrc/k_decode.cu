@@ -28,11 +28,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecArgs a) {
   constexpr int CG = DV / 4;          // column groups of 4
   constexpr int RG = kThreads / CG;   // row groups
   constexpr int RPT = DK / RG;        // rows per thread
-  __shared__ float s_pq[DK], s_pk[DK], s_eg[DK], s_q[DK], s_k[DK];
-  __shared__ float s_v[DV];
-  __shared__ float s_red[RG][DV];
+  // 16-byte alignment: s_v and s_red are accessed as float4
+  __shared__ __align__(16) float s_pq[DK], s_pk[DK], s_eg[DK], s_q[DK], s_k[DK];
+  __shared__ __align__(16) float s_v[DV];
+  __shared__ __align__(16) float s_red[RG][DV];
   __shared__ float s_z[kMaxM + kMaxW];
-  __shared__ float s_yw[2][DV];
   __shared__ int64_t s_pos;
 
   const int u = blockIdx.x;  // n * H + head
@@ -181,14 +181,240 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecArgs a) {
       __threadfence();
     }
   }
-  (void)s_yw;
+}
+
+// ------------------------------------------------------------------------------------
+// Split step for W <= kSplitMaxW: two kernels, each shaped for its own traffic.
+//  * decode_gla_kernel streams the fp32 state (128 KiB of the 166 KiB a unit moves):
+//    every thread issues its sixteen 16-byte state loads before anything else, three
+//    CTAs share an SM, and y_gla goes to y.
+//  * decode_win_kernel stages the two rings in shared memory, computes the window
+//    softmax (8 lanes per key, lanes interleaved over dimensions so the shared-memory
+//    reads are conflict-free), adds alpha * y_win into y, writes the new token into its
+//    slot and advances pos (last CTA of each sequence).
+// ------------------------------------------------------------------------------------
+constexpr int kSplitMaxW = 128;
+constexpr int kWinThreads = 256;
+constexpr int kWinWarps = kWinThreads / 32;
+
+template <typename T, int DK, int DV>
+__global__ void __launch_bounds__(kThreads, 3) decode_gla_kernel(DecArgs a) {
+  constexpr int CG = DV / 4;
+  constexpr int RG = kThreads / CG;
+  constexpr int RPT = DK / RG;
+  __shared__ __align__(16) float s_pq[DK], s_pk[DK], s_eg[DK];
+  __shared__ __align__(16) float s_v[DV];
+  __shared__ __align__(16) float s_red[RG][DV];
+  const int u = blockIdx.x;
+  const int tid = threadIdx.x;
+  float* h = a.h + (size_t)u * DK * DV;
+  const int cg = tid % CG, rg = tid / CG;
+  float4 hv[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i)
+    hv[i] = *reinterpret_cast<const float4*>(h + (size_t)(rg + RG * i) * DV + 4 * cg);
+  const T* pq = static_cast<const T*>(a.pq) + (size_t)u * DK;
+  const T* pk = static_cast<const T*>(a.pk) + (size_t)u * DK;
+  const float* lg = a.lg + (size_t)u * DK;
+  for (int d = tid; d < DK; d += kThreads) {
+    s_pq[d] = ld_f(pq + d);
+    s_pk[d] = ld_f(pk + d);
+    s_eg[d] = expf(lg[d]);
+  }
+  const T* vg = static_cast<const T*>(a.v) + (size_t)u * DV;
+  for (int c = tid; c < DV; c += kThreads) s_v[c] = ld_f(vg + c);
+  __syncthreads();
+  const float4 v4 = *reinterpret_cast<const float4*>(s_v + 4 * cg);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int r = rg + RG * i;
+    const float g = s_eg[r], b = s_pk[r], c = s_pq[r];
+    float4 x = hv[i];
+    x.x = fmaf(g, x.x, b * v4.x);
+    x.y = fmaf(g, x.y, b * v4.y);
+    x.z = fmaf(g, x.z, b * v4.z);
+    x.w = fmaf(g, x.w, b * v4.w);
+    *reinterpret_cast<float4*>(h + (size_t)r * DV + 4 * cg) = x;
+    acc.x = fmaf(c, x.x, acc.x);
+    acc.y = fmaf(c, x.y, acc.y);
+    acc.z = fmaf(c, x.z, acc.z);
+    acc.w = fmaf(c, x.w, acc.w);
+  }
+  *reinterpret_cast<float4*>(&s_red[rg][4 * cg]) = acc;
+  __syncthreads();
+  if (tid < DV) {
+    float yg = 0.f;
+#pragma unroll
+    for (int r = 0; r < RG; ++r) yg += s_red[r][tid];
+    static_cast<T*>(a.y)[(size_t)u * DV + tid] = cvt_out<T>(yg);
+  }
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gsrc)
+               : "memory");
+}
+
+template <typename T, int DK, int DV>
+__global__ void __launch_bounds__(kWinThreads) decode_win_kernel(DecArgs a) {
+  extern __shared__ __align__(128) unsigned char wsm[];
+  const int W = a.W, M = a.M;
+  // keys: W ring rows then M meta rows; values likewise, so one row index serves both
+  T* skey = reinterpret_cast<T*>(wsm);            // [W + M][DK]
+  T* sval = skey + (size_t)(W + M) * DK;          // [W + M][DV]
+  __shared__ __align__(16) float s_q[DK];
+  __shared__ float s_z[kMaxM + kSplitMaxW];
+  __shared__ int s_row[kMaxM + kSplitMaxW];
+  __shared__ float s_part[kWinThreads / DV > 0 ? kWinThreads / DV : 1][DV];
+  __shared__ int64_t s_pos;
+  const int u = blockIdx.x;
+  const int n = u / a.H, hh = u % a.H;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  T* kr = static_cast<T*>(a.kr) + (size_t)u * W * DK;
+  T* vr = static_cast<T*>(a.vr) + (size_t)u * W * DV;
+  const T* kg = static_cast<const T*>(a.k) + (size_t)u * DK;
+  const T* vg = static_cast<const T*>(a.v) + (size_t)u * DV;
+  if (tid == 0) s_pos = a.pos[n];
+  {
+    // asynchronous 16-byte copies of both rings and this head's meta rows
+    constexpr int KC = DK * sizeof(T) / 16, VC = DV * sizeof(T) / 16;  // 16-B chunks per row
+    const T* mkp = static_cast<const T*>(a.mk) + (size_t)hh * M * DK;
+    const T* mvp = static_cast<const T*>(a.mv) + (size_t)hh * M * DV;
+    for (int e = tid; e < W * KC; e += kWinThreads) cp_async16(skey + e * (16 / sizeof(T)), kr + e * (16 / sizeof(T)));
+    for (int e = tid; e < M * KC; e += kWinThreads)
+      cp_async16(skey + (size_t)W * DK + e * (16 / sizeof(T)), mkp + e * (16 / sizeof(T)));
+    for (int e = tid; e < W * VC; e += kWinThreads) cp_async16(sval + e * (16 / sizeof(T)), vr + e * (16 / sizeof(T)));
+    for (int e = tid; e < M * VC; e += kWinThreads)
+      cp_async16(sval + (size_t)W * DV + e * (16 / sizeof(T)), mvp + e * (16 / sizeof(T)));
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  const T* qg = static_cast<const T*>(a.q) + (size_t)u * DK;
+  T* y = static_cast<T*>(a.y) + (size_t)u * DV;
+  const float ygla = tid < DV ? ld_f(y + tid) : 0.f;  // y_gla from the previous kernel
+  for (int d = tid; d < DK; d += kWinThreads) s_q[d] = ld_f(qg + d);
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+  const int64_t p = s_pos;
+  const int slot = (int)(p % W);
+  // the new token replaces its slot, in shared memory and in the global ring
+  for (int d = tid; d < DK; d += kWinThreads) {
+    skey[(size_t)slot * DK + d] = kg[d];
+    kr[(size_t)slot * DK + d] = kg[d];
+  }
+  for (int c = tid; c < DV; c += kWinThreads) {
+    sval[(size_t)slot * DV + c] = vg[c];
+    vr[(size_t)slot * DV + c] = vg[c];
+  }
+  const int64_t t_lo = p - W + 1 > 0 ? p - W + 1 : 0;
+  const int nkeys = M + (int)(p - t_lo + 1);
+  // row of key j: meta keys first (rows W..W+M-1), then window token t_lo + i at slot
+  // (t_lo + i) mod W, computed as one wrap of s_lo + i
+  const int s_lo = (int)(t_lo % W);
+  for (int j = tid; j < nkeys; j += kWinThreads) {
+    const int i = j - M, r = s_lo + i;
+    s_row[j] = j < M ? W + j : (r >= W ? r - W : r);
+  }
+  __syncthreads();
+  {
+    // logits: 8 lanes per key, lane l8 takes dimensions {4*l8 + 32*i}
+    constexpr int LPK = 8;
+    const int sub = lane / LPK, l8 = lane % LPK;
+    for (int j0 = warp * 4; j0 < nkeys; j0 += kWinWarps * 4) {
+      const int j = j0 + sub;
+      float d = 0.f;
+      if (j < nkeys) {
+        const T* key = skey + (size_t)s_row[j] * DK;
+#pragma unroll
+        for (int e = 4 * l8; e < DK; e += 32) {
+          const float4 q4 = *reinterpret_cast<const float4*>(s_q + e);
+          const float4 k4 = ld4(key + e);
+          d = fmaf(q4.x, k4.x, d);
+          d = fmaf(q4.y, k4.y, d);
+          d = fmaf(q4.z, k4.z, d);
+          d = fmaf(q4.w, k4.w, d);
+        }
+      }
+#pragma unroll
+      for (int o = LPK / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      if (l8 == 0 && j < nkeys) s_z[j] = d * a.scale;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float mx = -INFINITY;
+    for (int j = lane; j < nkeys; j += 32) mx = fmaxf(mx, s_z[j]);
+    mx = warp_max(mx);
+    float sum = 0.f;
+    for (int j = lane; j < nkeys; j += 32) {
+      const float e = expf(s_z[j] - mx);
+      s_z[j] = e;
+      sum += e;
+    }
+    sum = warp_sum(sum);
+    const float inv = 1.f / sum;
+    for (int j = lane; j < nkeys; j += 32) s_z[j] *= inv;
+  }
+  __syncthreads();
+  constexpr int NP = kWinThreads / DV > 0 ? kWinThreads / DV : 1;  // key partitions
+  {
+    const int c = tid % DV, part = tid / DV;
+    if (part < NP) {
+      float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+      int j = part;
+      for (; j + 3 * NP < nkeys; j += 4 * NP) {
+        y0 = fmaf(s_z[j], ld_f(sval + (size_t)s_row[j] * DV + c), y0);
+        y1 = fmaf(s_z[j + NP], ld_f(sval + (size_t)s_row[j + NP] * DV + c), y1);
+        y2 = fmaf(s_z[j + 2 * NP], ld_f(sval + (size_t)s_row[j + 2 * NP] * DV + c), y2);
+        y3 = fmaf(s_z[j + 3 * NP], ld_f(sval + (size_t)s_row[j + 3 * NP] * DV + c), y3);
+      }
+      for (; j < nkeys; j += NP) y0 = fmaf(s_z[j], ld_f(sval + (size_t)s_row[j] * DV + c), y0);
+      s_part[part][c] = (y0 + y1) + (y2 + y3);
+    }
+  }
+  __syncthreads();
+  for (int c = tid; c < DV; c += kWinThreads) {
+    float ys = 0.f;
+#pragma unroll
+    for (int r = 0; r < NP; ++r) ys += s_part[r][c];
+    y[c] = cvt_out<T>(ygla + a.alpha * ys);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(&a.counters[n], 1u);
+    if (prev == (unsigned)a.H - 1) {
+      a.pos[n] = p + 1;
+      a.counters[n] = 0u;
+      __threadfence();
+    }
+  }
 }
 
 template <typename T, int D>
 cudaError_t launch_typed(const DecArgs& a, cudaStream_t s, int* launches) {
-  trace_begin("decode", s);
-  decode_kernel<T, D, D><<<a.N * a.H, kThreads, 0, s>>>(a);
-  trace_end(s);
+  if (a.W <= kSplitMaxW) {
+    // the window kernel reads y_gla written by the GLA kernel on the same stream
+    trace_begin("decode_gla", s);
+    decode_gla_kernel<T, D, D><<<a.N * a.H, kThreads, 0, s>>>(a);
+    trace_end(s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    const size_t smem = (size_t)(a.W + a.M) * 2 * D * sizeof(T);
+    e = cudaFuncSetAttribute(decode_win_kernel<T, D, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    trace_begin("decode_win", s);
+    decode_win_kernel<T, D, D><<<a.N * a.H, kWinThreads, smem, s>>>(a);
+    trace_end(s);
+  } else {
+    trace_begin("decode", s);
+    decode_kernel<T, D, D><<<a.N * a.H, kThreads, 0, s>>>(a);
+    trace_end(s);
+  }
   ++*launches;
   return cudaGetLastError();
 }
