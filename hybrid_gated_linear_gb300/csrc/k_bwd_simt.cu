@@ -130,26 +130,45 @@ __global__ void __launch_bounds__(kThreads) gla_bwd_kernel(BwdArgs a, BwdWs w) {
     if (tid < DK) {
       const int kk = tid;
       float run = 0.f;
-      for (int t = 0; t < kCB; ++t) {
-        float q = 0.f, k = 0.f, e = 1.f;
-        if (t < n) {
-          const size_t idx = (size_t)(t0 + t) * DK + kk;
-          run += lg[idx];
-          e = expf(run);
-          q = ld_f(pq + idx) * e;
-          k = ld_f(pk + idx) * expf(-run);
+      // eight tokens' loads in flight at a time
+      for (int t8 = 0; t8 < kCB; t8 += 8) {
+        float lv[8], qv[8], kv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const bool ok = t8 + i < n;
+          const size_t idx = (size_t)(t0 + t8 + i) * DK + kk;
+          lv[i] = ok ? lg[idx] : 0.f;
+          qv[i] = ok ? ld_f(pq + idx) : 0.f;
+          kv[i] = ok ? ld_f(pk + idx) : 0.f;
         }
-        Qt[t * (DK + 1) + kk] = q;
-        Kt[t * (DK + 1) + kk] = k;
-        Eb[t * (DK + 1) + kk] = e;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int t = t8 + i;
+          run += lv[i];
+          const float e = t < n ? expf(run) : 1.f;
+          Qt[t * (DK + 1) + kk] = qv[i] * e;
+          Kt[t * (DK + 1) + kk] = t < n ? kv[i] * expf(-run) : 0.f;
+          Eb[t * (DK + 1) + kk] = e;
+        }
       }
       eG[kk] = expf(run);
     }
-    for (int e = tid; e < kCB * DV; e += kThreads) {
+    constexpr int kPer = kCB * DV / kThreads;  // elements per thread
+    float vv[kPer], dd[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = tid + i * kThreads;
       const int t = e / DV, c = e % DV;
       const bool ok = t < n;
-      Vs[t * (DV + 1) + c] = ok ? ld_f(vg + (size_t)(t0 + t) * DV + c) : 0.f;
-      if (want_dy) dYs[t * (DV + 1) + c] = ok ? ld_f(dyg + (size_t)(t0 + t) * DV + c) : 0.f;
+      vv[i] = ok ? ld_f(vg + (size_t)(t0 + t) * DV + c) : 0.f;
+      dd[i] = (ok && want_dy) ? ld_f(dyg + (size_t)(t0 + t) * DV + c) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = tid + i * kThreads;
+      const int t = e / DV, c = e % DV;
+      Vs[t * (DV + 1) + c] = vv[i];
+      if (want_dy) dYs[t * (DV + 1) + c] = dd[i];
     }
   };
 
@@ -160,9 +179,13 @@ __global__ void __launch_bounds__(kThreads) gla_bwd_kernel(BwdArgs a, BwdWs w) {
   }
   __syncthreads();
   for (int ch = 0; ch < nc; ++ch) {
-    for (int e = tid; e < DK * DV; e += kThreads) {
-      const int r = e / DV, c = e % DV;
-      states[(size_t)ch * DK * DV + e] = Hs[r * (DV + 1) + c];
+    {
+      float4* dst = reinterpret_cast<float4*>(states + (size_t)ch * DK * DV);
+      for (int e4 = tid; e4 < DK * DV / 4; e4 += kThreads) {
+        const int e = 4 * e4, r = e / DV, c = e % DV;
+        const float* src = Hs + r * (DV + 1) + c;
+        dst[e4] = make_float4(src[0], src[1], src[2], src[3]);
+      }
     }
     load_chunk(ch, false);
     __syncthreads();
@@ -181,9 +204,26 @@ __global__ void __launch_bounds__(kThreads) gla_bwd_kernel(BwdArgs a, BwdWs w) {
   for (int ch = nc - 1; ch >= 0; --ch) {
     const int t0 = ch * kCB;
     const int n = min(kCB, L - t0);
-    for (int e = tid; e < DK * DV; e += kThreads) {
-      const int r = e / DV, c = e % DV;
-      Hs[r * (DV + 1) + c] = states[(size_t)ch * DK * DV + e];
+    {
+      // the saved state of this chunk: 16-byte loads, eight in flight per thread
+      const float4* src = reinterpret_cast<const float4*>(states + (size_t)ch * DK * DV);
+      constexpr int kN4 = DK * DV / 4 / kThreads;
+#pragma unroll
+      for (int b8 = 0; b8 < kN4; b8 += 8) {
+        float4 r4[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r4[i] = src[tid + (b8 + i) * kThreads];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int e = 4 * (tid + (b8 + i) * kThreads);
+          const int r = e / DV, c = e % DV;
+          float* dst = Hs + r * (DV + 1) + c;
+          dst[0] = r4[i].x;
+          dst[1] = r4[i].y;
+          dst[2] = r4[i].z;
+          dst[3] = r4[i].w;
+        }
+      }
     }
     load_chunk(ch, true);
     __syncthreads();
