@@ -17,6 +17,8 @@
 // query (dq, and the row statistics lse_i and D_i = dyw_i . y_win_i) and one per key
 // (dk, dv, visiting the <= W queries that see the key); meta-key/value gradients are
 // per-token terms reduced over (batch, token) in a fixed order.
+#include <type_traits>
+
 #include "lizard_dev.cuh"
 #include "lizard_internal.h"
 
@@ -28,7 +30,8 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
 struct BwdWs {
-  float* states;   // [BH][nc][DK][DV] state at the start of each chunk
+  float* states;   // [BH][nc][DK][DV] state at the start of each chunk (CUDA-core path)
+  unsigned char* gla_tc;  // scratch of the tensor-core GLA path
   float* dvacc;    // [BH][L][DV] GLA part of dv
   float* lse;      // [BH][L]
   float* Dw;       // [BH][L]
@@ -45,7 +48,9 @@ inline int bwd_nsplit(int B, int H, int L) {
   return ns < 1 ? 1 : ns;
 }
 
-BwdWs carve(unsigned char* p, int B, int H, int L, int dk, int dv, int M) {
+// Window scratch and the GLA part of dv first, then the GLA path's own scratch: the
+// chunk states (CUDA cores) or bwd_gla_tc_workspace bytes (tensor cores).
+BwdWs carve(unsigned char* p, int B, int H, int L, int dk, int dv, int M, bool tc) {
   BwdWs w;
   const size_t BH = (size_t)B * H;
   const size_t nc = (L + kCB - 1) / kCB;
@@ -55,7 +60,6 @@ BwdWs carve(unsigned char* p, int B, int H, int L, int dk, int dv, int M) {
     off += align_up(floats * sizeof(float) + 1, 256);
     return r;
   };
-  w.states = take(BH * nc * dk * dv);
   w.dvacc = take(BH * (size_t)L * dv);
   w.lse = take(BH * (size_t)L);
   w.Dw = take(BH * (size_t)L);
@@ -63,7 +67,10 @@ BwdWs carve(unsigned char* p, int B, int H, int L, int dk, int dv, int M) {
   w.p_meta = take(BH * (size_t)L * M);
   w.nsplit = bwd_nsplit(B, H, L);
   w.dmeta_part = take((size_t)w.nsplit * H * M * (dk + dv));
-  (void)off;
+  w.states = nullptr;
+  w.gla_tc = nullptr;
+  if (tc) w.gla_tc = p + off;
+  else w.states = take(BH * nc * dk * dv);
   return w;
 }
 
@@ -72,14 +79,15 @@ size_t carve_bytes(int B, int H, int L, int dk, int dv, int M) {
   const size_t nc = (L + kCB - 1) / kCB;
   size_t off = 0;
   auto take = [&](size_t floats) { off += align_up(floats * sizeof(float) + 1, 256); };
-  take(BH * nc * dk * dv);
   take(BH * (size_t)L * dv);
   take(BH * (size_t)L);
   take(BH * (size_t)L);
   take(BH * (size_t)L * M);
   take(BH * (size_t)L * M);
   take((size_t)bwd_nsplit(B, H, L) * H * M * (dk + dv));
-  return off;
+  const size_t simt = align_up(BH * nc * dk * dv * sizeof(float) + 1, 256);
+  const size_t tc = dk == 128 && dv == 128 && L > 0 ? bwd_gla_tc_workspace((int)BH, L) : 0;
+  return off + (simt > tc ? simt : tc);
 }
 
 // ------------------------------------------------------------------------------------
@@ -539,10 +547,14 @@ __global__ void dmeta_final_kernel(BwdArgs a, BwdWs w) {
 
 template <typename T, int D>
 cudaError_t launch_typed(const BwdArgs& a, cudaStream_t s, int* launches) {
-  BwdWs w = carve(a.ws, a.B, a.H, a.L, D, D, a.M);
+  constexpr lizard_dtype kDt = std::is_same<T, bf16>::value ? LIZARD_BF16 : LIZARD_F32;
+  const bool tc = bwd_gla_tc_supported(D, D, a.L, kDt);
+  BwdWs w = carve(a.ws, a.B, a.H, a.L, D, D, a.M, tc);
   const int BH = a.B * a.H;
   cudaError_t e;
-  {
+  if (tc) {
+    if ((e = launch_bwd_gla_tc(a, w.dvacc, w.gla_tc, s, launches)) != cudaSuccess) return e;
+  } else {
     const size_t smem = gla_bwd_smem_floats<D, D>() * sizeof(float);
     e = cudaFuncSetAttribute(gla_bwd_kernel<T, D, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);

@@ -1,0 +1,716 @@
+// k_bwd_tc.cu -- backward of the GLA branch on tcgen05 tensor cores (bf16, d = 128).
+//
+// The pages give no backward formulas; this is the exact adjoint of the chunkwise forward
+// ("Lizard", arXiv 2507.09025, Method: parallel form with cumulative gate products), laid
+// out so that every chunk is independent once two linear scans over the chunk states are
+// done.  Chunks hold C = 128 tokens; b is the chunk-local inclusive cumsum of log gamma,
+// Gamma its last value, Qt = phi_q e^b, Kt = phi_k e^-b, h_c the state at the start of
+// chunk c and G_c the adjoint of the state at its end.
+//
+//   1. prep   (CUDA cores)  Qt, Kt and e^b in bf16, Gamma in fp32.
+//   2. scan   (tcgen05)     h_{c+1} = diag(e^Gamma_c) (h_c + Kt_c^T V_c),  h_0 = h0
+//                           G_{c-1} = diag(e^Gamma_c) G_c + Qt_c^T dY_c,   G_{nc-1} = 0
+//                           stored as bf16 h_c and Gt_c = diag(e^Gamma_c) G_c.  One CTA per
+//                           (b, h, 32 dv columns, direction): the 128 x 32 chunk products
+//                           come from the tensor cores, the scans run in fp32 registers.
+//                           G_{-1} is the adjoint of h0.
+//   3. chunk  (tcgen05)     per (b, h, chunk), every product M = N = K = 128:
+//                             A = dY V^T,  P = Qt Kt^T        (masked to s <= t, bf16)
+//                             dQt = dY h^T + A Kt,   dKt = V Gt^T + A^T Qt
+//                             dV  = Kt Gt + P^T dY
+//                           then d phi_q = dQt e^b, d phi_k = dKt e^-b, and the per-token
+//                           log-gate term r = phi_q d phi_q - phi_k d phi_k = Qt dQt - Kt dKt
+//                           with its sum over the chunk's tokens.
+//   4. suffix (CUDA cores)  d log gamma_t = sum_{t' >= t} r_t'.
+//
+// Every wait is bounded; on a timeout the CTA records LIZARD_ERR_TIMEOUT in the status
+// word, drains its copies and MMAs, frees its tensor memory and returns.
+#include "lizard_dev.cuh"
+#include "lizard_internal.h"
+#include "tc_sm100.cuh"
+
+namespace lz {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 128;   // chunk
+constexpr int kD = 128;   // dk = dv
+constexpr int kSl = 32;   // dv columns per scan CTA
+constexpr int kSlices = kD / kSl;
+constexpr uint64_t kWaitNs = 1000000000ull;      // 1 s for the exit drains
+constexpr long long kWaitCycles = 2000000000ll;  // ~1 s of SM clock per wait
+constexpr float kMaxLogSum = 80.f;  // |chunk-local log-gate sum| beyond which e^{+-b} overflows
+
+struct GlaWs {
+  bf16 *qt, *kt, *eb;  // [BH][L][128]
+  float* gam;          // [BH][nc][128]
+  bf16 *hs, *gs;       // [BH][nc][128][128]
+  float* rtot;         // [BH][nc][128]
+};
+
+size_t gla_ws_layout(int BH, int L, unsigned char* p, GlaWs* w) {
+  const size_t nc = (L + kC - 1) / kC;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    unsigned char* r = p ? p + off : nullptr;
+    off += align_up(bytes, 256);
+    return r;
+  };
+  const size_t tok = (size_t)BH * L * kD * sizeof(bf16);
+  const size_t st = (size_t)BH * nc * kD * kD * sizeof(bf16);
+  const size_t vec = (size_t)BH * nc * kD * sizeof(float);
+  GlaWs g;
+  g.qt = reinterpret_cast<bf16*>(take(tok));
+  g.kt = reinterpret_cast<bf16*>(take(tok));
+  g.eb = reinterpret_cast<bf16*>(take(tok));
+  g.gam = reinterpret_cast<float*>(take(vec));
+  g.hs = reinterpret_cast<bf16*>(take(st));
+  g.gs = reinterpret_cast<bf16*>(take(st));
+  g.rtot = reinterpret_cast<float*>(take(vec));
+  if (w) *w = g;
+  return off;
+}
+
+template <int NB>
+struct CtlT {
+  uint64_t bar[NB];
+  uint32_t tmem;
+  int abort;
+};
+
+// Bounded wait: gives up (and raises the CTA's abort flag) after kWaitCycles SM clock
+// cycles, or as soon as another role aborted.
+template <int NB>
+__device__ __forceinline__ bool wait_bar(CtlT<NB>* ctl, int i, uint32_t parity) {
+  uint64_t* b = &ctl->bar[i];
+  if (mbar_try_wait(b, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+#pragma unroll 1
+    for (int k = 0; k < 32; ++k)
+      if (mbar_try_wait(b, parity)) return true;
+    if (*(volatile int*)&ctl->abort) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *(volatile int*)&ctl->abort = 1;
+      return false;
+    }
+  }
+}
+
+// Waits, with a time limit of its own, for the last armed phase of a barrier; used only
+// while leaving.
+template <int NB>
+__device__ __forceinline__ void drain_bar(CtlT<NB>* ctl, int i, uint32_t armed, uint64_t t0) {
+  if (armed == 0) return;
+  while (!mbar_try_wait(&ctl->bar[i], (armed - 1) & 1))
+    if (globaltimer_ns() - t0 > kWaitNs) break;
+}
+
+// K-major SW128 operand descriptor for k-step j (16 elements) of a 128-row tile stored as
+// two 64-column blocks.
+__device__ __forceinline__ uint64_t desc_k(uint32_t base, int j) {
+  return smem_desc(base + (uint32_t)((j * 16) >> 6) * (kC * 128u) + (uint32_t)((j * 16) & 63) * 2u,
+                   16, 1024, kSw128);
+}
+
+// MN-major SW128 operand descriptor for k-step j of the same tile read transposed: the
+// tile's rows are the K index, its 128 columns the M (or N) index.
+__device__ __forceinline__ uint64_t desc_mn(uint32_t base, int j) {
+  return smem_desc(base + (uint32_t)j * 2048u, kC * 128u, 1024, kSw128);
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Sums v over the 32 lanes of the warp entry by entry; afterwards lane l holds the total
+// of entry l (reduce-scatter by recursive halving, a fixed order).
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < o; ++k) {
+      const float send = upper ? v[k] : v[k + o];
+      const float keep = upper ? v[k + o] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0];
+}
+
+// ------------------------------------------------------------------------------------
+// 1. prep: one CTA per (chunk, b*h), thread = key dimension.
+// ------------------------------------------------------------------------------------
+struct PrepP {
+  int L, nc;
+  const bf16 *pq, *pk;
+  const float* lg;
+  GlaWs w;
+  unsigned* status;
+};
+
+__global__ void __launch_bounds__(kD) prep_kernel(const PrepP p) {
+  const int c = blockIdx.x, bh = blockIdx.y, i = threadIdx.x;
+  const int L = p.L, t0 = c * kC, n = min(kC, L - t0);
+  const size_t base = ((size_t)bh * L + t0) * kD + i;
+  const bf16* pq = p.pq + base;
+  const bf16* pk = p.pk + base;
+  const float* lg = p.lg + base;
+  bf16* qt = p.w.qt + base;
+  bf16* kt = p.w.kt + base;
+  bf16* eb = p.w.eb + base;
+  float run = 0.f, big = 0.f;
+  for (int t8 = 0; t8 < n; t8 += 8) {
+    float lv[8], qv[8], kv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool ok = t8 + u < n;
+      const size_t o = (size_t)(t8 + u) * kD;
+      lv[u] = ok ? lg[o] : 0.f;
+      qv[u] = ok ? __bfloat162float(pq[o]) : 0.f;
+      kv[u] = ok ? __bfloat162float(pk[o]) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (t8 + u < n) {
+        run += lv[u];
+        big = fmaxf(big, fabsf(run));
+        const float e = __expf(run);
+        const size_t o = (size_t)(t8 + u) * kD;
+        qt[o] = __float2bfloat16_rn(qv[u] * e);
+        kt[o] = __float2bfloat16_rn(kv[u] * __expf(-run));
+        eb[o] = __float2bfloat16_rn(e);
+      }
+    }
+  }
+  p.w.gam[((size_t)bh * p.nc + c) * kD + i] = run;
+  // e^{+-b} must stay inside the fp32/bf16 range for the factorised form.
+  if (big > kMaxLogSum) raise_status(p.status, kDevCheck);
+}
+
+// ------------------------------------------------------------------------------------
+// 2. scan: one CTA per (b*h, 32-column slice, direction); warp 0 TMA, warp 1 MMA,
+//    warps 2-5 scan (thread = state row).
+// ------------------------------------------------------------------------------------
+struct ScanMaps {
+  CUtensorMap x0, y0, x1, y1;  // direction 0: Kt, V ; direction 1: Qt, dY
+};
+
+struct ScanP {
+  int L, nc;
+  const float* h0;
+  float* dh0;
+  GlaWs w;
+  unsigned* status;
+};
+
+enum { S_FULL = 0, S_EMPTY = 2, S_DFULL = 4, S_DFREE = 6, S_DONE = 8, S_COUNT };
+constexpr uint32_t kScanX = kC * kD * 2;             // 32 KB: Kt or Qt tile
+constexpr uint32_t kScanY = kC * kSl * 2;            // 8 KB: V or dY slice
+constexpr uint32_t kScanStage = kScanX + kScanY;     // multiple of 1024
+constexpr uint32_t kScanBars = 2 * kScanStage;
+constexpr size_t kScanSmem = kScanBars + 1024 + 1024;
+constexpr int kScanThreads = 6 * 32;
+
+__global__ void __launch_bounds__(kScanThreads, 1)
+scan_kernel(const __grid_constant__ ScanMaps maps, const ScanP p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  using Ctl = CtlT<S_COUNT>;
+  Ctl* ctl = reinterpret_cast<Ctl*>(sm + kScanBars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int dir = blockIdx.x & 1;
+  const int sl = (blockIdx.x >> 1) % kSlices;
+  const int bh = blockIdx.x / (2 * kSlices);
+  const int nc = p.nc;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S_COUNT; ++i)
+      mbar_init(&ctl->bar[i], (i == S_DFREE || i == S_DFREE + 1) ? 128u : 1u);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem, 64);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const CUtensorMap* mx = dir ? &maps.x1 : &maps.x0;
+      const CUtensorMap* my = dir ? &maps.y1 : &maps.y0;
+      uint32_t armed0 = 0, armed1 = 0;
+      bool ok = true;
+      for (int u = 0; u < nc && ok; ++u) {
+        const int c = dir ? nc - 1 - u : u, s = u & 1;
+        if (u >= 2 && !(ok = wait_bar(ctl, S_EMPTY + s, ((u >> 1) - 1) & 1))) break;
+        unsigned char* st = sm + s * kScanStage;
+        mbar_arrive_expect_tx(&ctl->bar[S_FULL + s], kScanStage);
+        tma_load_3d(st, mx, 0, c * kC, bh, &ctl->bar[S_FULL + s]);
+        tma_load_3d(st + kScanX / 2, mx, 64, c * kC, bh, &ctl->bar[S_FULL + s]);
+        tma_load_3d(st + kScanX, my, sl * kSl, c * kC, bh, &ctl->bar[S_FULL + s]);
+        if (s) ++armed1;
+        else ++armed0;
+      }
+      if (!ok) ctl->abort = 1;
+      const uint64_t t0 = globaltimer_ns();
+      drain_bar(ctl, S_FULL, armed0, t0);
+      drain_bar(ctl, S_FULL + 1, armed1, t0);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // D[i][j] = sum_s X[s][i] Y[s][j]: A = X^T (MN-major), B = Y slice (MN-major, 64 B rows)
+      const uint32_t id = idesc_bf16(kD, kSl, true, true);
+      const uint32_t sbase = smem_u32(sm);
+      bool ok = true;
+      for (int u = 0; u < nc && ok; ++u) {
+        const int s = u & 1;
+        if (!(ok = wait_bar(ctl, S_FULL + s, (u >> 1) & 1))) break;
+        if (u >= 2 && !(ok = wait_bar(ctl, S_DFREE + s, ((u >> 1) - 1) & 1))) break;
+        tc_fence_after();
+        const uint32_t xb = sbase + s * kScanStage, yb = xb + kScanX;
+        for (int j = 0; j < kC / 16; ++j)
+          mma_bf16(tmem + s * kSl, desc_mn(xb, j), smem_desc(yb + j * 1024, kC * 64, 512, kSw64),
+                   id, j > 0);
+        mma_commit(&ctl->bar[S_EMPTY + s]);
+        mma_commit(&ctl->bar[S_DFULL + s]);
+      }
+      if (!ok) ctl->abort = 1;
+      mma_commit(&ctl->bar[S_DONE]);
+      drain_bar(ctl, S_DONE, 1, globaltimer_ns());
+    }
+  } else {
+    const int qw = warp & 3;
+    const int i = qw * 32 + lane;  // state row = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(qw * 32) << 16);
+    float x[kSl];
+    if (dir == 0 && p.h0) {
+      const float4* src = reinterpret_cast<const float4*>(p.h0 + ((size_t)bh * kD + i) * kD + sl * kSl);
+#pragma unroll
+      for (int k = 0; k < kSl / 4; ++k) {
+        const float4 v = src[k];
+        x[4 * k] = v.x;
+        x[4 * k + 1] = v.y;
+        x[4 * k + 2] = v.z;
+        x[4 * k + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < kSl; ++k) x[k] = 0.f;
+    }
+    bf16* outb = dir ? p.w.gs : p.w.hs;
+    bool ok = true;
+    for (int u = 0; u < nc && ok; ++u) {
+      const int c = dir ? nc - 1 - u : u, s = u & 1;
+      const float g = expf(p.w.gam[((size_t)bh * nc + c) * kD + i]);
+      if (!(ok = wait_bar(ctl, S_DFULL + s, (u >> 1) & 1))) break;
+      tc_fence_after();
+      uint32_t d[kSl];
+      tmem_ld32(tl + s * kSl, d);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&ctl->bar[S_DFREE + s]);
+      if (dir) {
+#pragma unroll
+        for (int k = 0; k < kSl; ++k) x[k] *= g;
+      }
+      uint4* dst = reinterpret_cast<uint4*>(outb + (((size_t)bh * nc + c) * kD + i) * kD + sl * kSl);
+#pragma unroll
+      for (int k = 0; k < kSl / 8; ++k)
+        dst[k] = make_uint4(pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
+                            pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
+      if (dir) {
+#pragma unroll
+        for (int k = 0; k < kSl; ++k) x[k] += __uint_as_float(d[k]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < kSl; ++k) x[k] = g * (x[k] + __uint_as_float(d[k]));
+      }
+    }
+    if (!ok) ctl->abort = 1;
+    if (ok && dir == 1 && p.dh0) {
+      float4* dst = reinterpret_cast<float4*>(p.dh0 + ((size_t)bh * kD + i) * kD + sl * kSl);
+#pragma unroll
+      for (int k = 0; k < kSl / 4; ++k) dst[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+  if (threadIdx.x == 0 && ctl->abort) raise_status(p.status, kDevTimeout);
+}
+
+// ------------------------------------------------------------------------------------
+// 3. chunk: one CTA per (b*h, chunk); warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+//    (thread = tile row, half of the columns).
+// ------------------------------------------------------------------------------------
+struct ChunkMaps {
+  CUtensorMap dy, v, qt, kt, hs, gs;
+};
+
+struct ChunkP {
+  int L, nc;
+  const bf16* eb;
+  bf16 *dpq, *dpk;
+  float* dlg;
+  float* dvacc;
+  float* rtot;
+  unsigned* status;
+};
+
+enum {
+  M_LD0 = 0, M_LD1, M_LD2, M_LD3, M_A, M_P, M_AS, M_PS, M_DQK, M_DV, M_DONE, M_COUNT
+};
+constexpr uint32_t kTile = kC * kD * 2;  // 32 KB
+constexpr uint32_t C_DY = 0, C_V = kTile, C_QT = 2 * kTile, C_KT = 3 * kTile, C_HS = 4 * kTile,
+                   C_GS = 5 * kTile, C_RED = 6 * kTile, C_BARS = C_RED + 2048;
+constexpr size_t kChunkSmem = C_BARS + 1024 + 1024;
+constexpr int kChunkThreads = 10 * 32;
+constexpr int kEpiThreads = 8 * 32;
+// TMEM columns
+constexpr uint32_t T_A = 0, T_P = 128, T_DQ = 256, T_DK = 384;
+
+__global__ void __launch_bounds__(kChunkThreads, 1)
+chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  using Ctl = CtlT<M_COUNT>;
+  Ctl* ctl = reinterpret_cast<Ctl*>(sm + C_BARS);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nc = p.nc, L = p.L;
+  const int c = blockIdx.x % nc, bh = blockIdx.x / nc;
+  const int t0 = c * kC, n = min(kC, L - t0);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < M_COUNT; ++i)
+      mbar_init(&ctl->bar[i], (i == M_AS || i == M_PS) ? (uint32_t)kEpiThreads : 1u);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const int zs = bh * nc + c;
+      mbar_arrive_expect_tx(&ctl->bar[M_LD0], 2 * kTile);
+      tma_load_3d(sm + C_DY, &maps.dy, 0, t0, bh, &ctl->bar[M_LD0]);
+      tma_load_3d(sm + C_DY + kTile / 2, &maps.dy, 64, t0, bh, &ctl->bar[M_LD0]);
+      tma_load_3d(sm + C_HS, &maps.hs, 0, 0, zs, &ctl->bar[M_LD0]);
+      tma_load_3d(sm + C_HS + kTile / 2, &maps.hs, 64, 0, zs, &ctl->bar[M_LD0]);
+      mbar_arrive_expect_tx(&ctl->bar[M_LD1], kTile);
+      tma_load_3d(sm + C_V, &maps.v, 0, t0, bh, &ctl->bar[M_LD1]);
+      tma_load_3d(sm + C_V + kTile / 2, &maps.v, 64, t0, bh, &ctl->bar[M_LD1]);
+      mbar_arrive_expect_tx(&ctl->bar[M_LD2], kTile);
+      tma_load_3d(sm + C_GS, &maps.gs, 0, 0, zs, &ctl->bar[M_LD2]);
+      tma_load_3d(sm + C_GS + kTile / 2, &maps.gs, 64, 0, zs, &ctl->bar[M_LD2]);
+      mbar_arrive_expect_tx(&ctl->bar[M_LD3], 2 * kTile);
+      tma_load_3d(sm + C_QT, &maps.qt, 0, t0, bh, &ctl->bar[M_LD3]);
+      tma_load_3d(sm + C_QT + kTile / 2, &maps.qt, 64, t0, bh, &ctl->bar[M_LD3]);
+      tma_load_3d(sm + C_KT, &maps.kt, 0, t0, bh, &ctl->bar[M_LD3]);
+      tma_load_3d(sm + C_KT + kTile / 2, &maps.kt, 64, t0, bh, &ctl->bar[M_LD3]);
+      const uint64_t tw = globaltimer_ns();
+      for (int b = M_LD0; b <= M_LD3; ++b) drain_bar(ctl, b, 1, tw);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_kk = idesc_bf16(kC, kD, false, false);
+      const uint32_t id_kn = idesc_bf16(kC, kD, false, true);
+      const uint32_t id_nn = idesc_bf16(kC, kD, true, true);
+      const uint32_t sb = smem_u32(sm);
+      auto mma_kk = [&](uint32_t d, uint32_t a, uint32_t b, bool acc) {
+        for (int j = 0; j < 8; ++j) mma_bf16(tmem + d, desc_k(a, j), desc_k(b, j), id_kk, acc || j > 0);
+      };
+      auto mma_kn = [&](uint32_t d, uint32_t a, uint32_t b, bool acc) {
+        for (int j = 0; j < 8; ++j) mma_bf16(tmem + d, desc_k(a, j), desc_mn(b, j), id_kn, acc || j > 0);
+      };
+      auto mma_nn = [&](uint32_t d, uint32_t a, uint32_t b, bool acc) {
+        for (int j = 0; j < 8; ++j) mma_bf16(tmem + d, desc_mn(a, j), desc_mn(b, j), id_nn, acc || j > 0);
+      };
+      bool ok = wait_bar(ctl, M_LD0, 0);
+      if (ok) {
+        tc_fence_after();
+        mma_kk(T_DQ, sb + C_DY, sb + C_HS, false);  // dQt  = dY h^T
+      }
+      if (ok && (ok = wait_bar(ctl, M_LD1, 0))) {
+        tc_fence_after();
+        mma_kk(T_A, sb + C_DY, sb + C_V, false);    // A    = dY V^T
+        mma_commit(&ctl->bar[M_A]);                 // (h tile free)
+      }
+      if (ok && (ok = wait_bar(ctl, M_LD2, 0))) {
+        tc_fence_after();
+        mma_kk(T_DK, sb + C_V, sb + C_GS, false);   // dKt  = V Gt^T
+      }
+      if (ok && (ok = wait_bar(ctl, M_LD3, 0))) {
+        tc_fence_after();
+        mma_kk(T_P, sb + C_QT, sb + C_KT, false);   // P    = Qt Kt^T
+        mma_commit(&ctl->bar[M_P]);                 // (V tile free)
+      }
+      if (ok && (ok = wait_bar(ctl, M_AS, 0))) {
+        tc_fence_after();
+        mma_kn(T_DQ, sb + C_HS, sb + C_KT, true);   // dQt += A Kt
+        mma_nn(T_DK, sb + C_HS, sb + C_QT, true);   // dKt += A^T Qt
+        mma_commit(&ctl->bar[M_DQK]);
+        mma_kn(T_A, sb + C_KT, sb + C_GS, false);   // dV   = Kt Gt
+      }
+      if (ok && (ok = wait_bar(ctl, M_PS, 0))) {
+        tc_fence_after();
+        mma_nn(T_A, sb + C_V, sb + C_DY, true);     // dV  += P^T dY
+        mma_commit(&ctl->bar[M_DV]);
+      }
+      if (!ok) ctl->abort = 1;
+      mma_commit(&ctl->bar[M_DONE]);
+      drain_bar(ctl, M_DONE, 1, globaltimer_ns());
+    }
+  } else {
+    const int ew = warp - 2;      // 0..7
+    const int qw = warp & 3;      // TMEM lane quarter
+    const int hf = ew >> 2;       // column half
+    const int t = qw * 32 + lane; // tile row
+    const bool valid = t < n;
+    const uint32_t tl = tmem + ((uint32_t)(qw * 32) << 16);
+    float* red = reinterpret_cast<float*>(sm + C_RED);  // [4][128] column partials of r
+    bool ok = true;
+
+    // Masked (s <= t) bf16 copy of an M = N = 128 product, K-major rows t.
+    auto mask_store = [&](uint32_t tcol, unsigned char* dst) {
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        uint32_t r[32];
+        tmem_ld32(tl + tcol + 64 * hf + 32 * g, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int s0 = 64 * hf + 32 * g + 8 * m;
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int s = s0 + 2 * e;
+            w[e] = pack_bf16x2(s <= t ? __uint_as_float(r[8 * m + 2 * e]) : 0.f,
+                               s + 1 <= t ? __uint_as_float(r[8 * m + 2 * e + 1]) : 0.f);
+          }
+          *reinterpret_cast<uint4*>(dst + sw128_offset(t, s0, kC)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    };
+
+    if ((ok = wait_bar(ctl, M_A, 0))) {
+      tc_fence_after();
+      mask_store(T_A, sm + C_HS);
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();
+    mbar_arrive(&ctl->bar[M_AS]);
+    if (ok && (ok = wait_bar(ctl, M_P, 0))) {
+      tc_fence_after();
+      mask_store(T_P, sm + C_V);
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();
+    mbar_arrive(&ctl->bar[M_PS]);
+
+    // d phi_q, d phi_k and the log-gate term
+    if (ok && (ok = wait_bar(ctl, M_DQK, 0))) {
+      tc_fence_after();
+      const size_t row = (size_t)bh * L + t0 + t;
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {
+        const int i0 = 64 * hf + 32 * g;
+        uint32_t dq[32], dk[32];
+        tmem_ld32(tl + T_DQ + i0, dq);
+        tmem_ld32(tl + T_DK + i0, dk);
+        uint4 ebv[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          ebv[m] = valid ? reinterpret_cast<const uint4*>(p.eb + row * kD + i0)[m] : make_uint4(0, 0, 0, 0);
+        tmem_ld_wait();
+        float rr[32];
+        uint4 oq[4], ok4[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const uint4 qv = *reinterpret_cast<const uint4*>(sm + C_QT + sw128_offset(t, i0 + 8 * m, kC));
+          const uint4 kv = *reinterpret_cast<const uint4*>(sm + C_KT + sw128_offset(t, i0 + 8 * m, kC));
+          const uint32_t qa[4] = {qv.x, qv.y, qv.z, qv.w};
+          const uint32_t ka[4] = {kv.x, kv.y, kv.z, kv.w};
+          const uint32_t ea[4] = {ebv[m].x, ebv[m].y, ebv[m].z, ebv[m].w};
+          uint32_t wq[4], wk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k0 = 8 * m + 2 * e;
+            const float q0 = __uint_as_float(dq[k0]), q1 = __uint_as_float(dq[k0 + 1]);
+            const float d0 = __uint_as_float(dk[k0]), d1 = __uint_as_float(dk[k0 + 1]);
+            const float e0 = bf_lo(ea[e]), e1 = bf_hi(ea[e]);
+            wq[e] = pack_bf16x2(q0 * e0, q1 * e1);
+            wk[e] = pack_bf16x2(valid ? __fdividef(d0, e0) : 0.f, valid ? __fdividef(d1, e1) : 0.f);
+            rr[k0] = valid ? bf_lo(qa[e]) * q0 - bf_lo(ka[e]) * d0 : 0.f;
+            rr[k0 + 1] = valid ? bf_hi(qa[e]) * q1 - bf_hi(ka[e]) * d1 : 0.f;
+          }
+          oq[m] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+          ok4[m] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+        }
+        if (valid) {
+          uint4* dq_out = reinterpret_cast<uint4*>(p.dpq + row * kD + i0);
+          uint4* dk_out = reinterpret_cast<uint4*>(p.dpk + row * kD + i0);
+          float4* r_out = reinterpret_cast<float4*>(p.dlg + row * kD + i0);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            dq_out[m] = oq[m];
+            dk_out[m] = ok4[m];
+          }
+#pragma unroll
+          for (int m = 0; m < 8; ++m) r_out[m] = make_float4(rr[4 * m], rr[4 * m + 1], rr[4 * m + 2], rr[4 * m + 3]);
+        }
+        red[qw * kD + i0 + lane] = warp_reduce_scatter32(rr, lane);
+      }
+    }
+    // all 256 epilogue threads meet here exactly once, whatever happened above
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+    if (ok && ew < 4) {
+      const int col = ew * 32 + lane;
+      p.rtot[((size_t)bh * nc + c) * kD + col] =
+          red[col] + red[kD + col] + red[2 * kD + col] + red[3 * kD + col];
+    }
+
+    // GLA part of dv
+    if (ok && (ok = wait_bar(ctl, M_DV, 0))) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {
+        const int i0 = 64 * hf + 32 * g;
+        uint32_t r[32];
+        tmem_ld32(tl + T_A + i0, r);
+        tmem_ld_wait();
+        if (valid) {
+          float4* dst = reinterpret_cast<float4*>(p.dvacc + ((size_t)bh * L + t0 + t) * kD + i0);
+#pragma unroll
+          for (int m = 0; m < 8; ++m)
+            dst[m] = make_float4(__uint_as_float(r[4 * m]), __uint_as_float(r[4 * m + 1]),
+                                 __uint_as_float(r[4 * m + 2]), __uint_as_float(r[4 * m + 3]));
+        }
+      }
+    }
+    if (!ok) ctl->abort = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && ctl->abort) raise_status(p.status, kDevTimeout);
+}
+
+// ------------------------------------------------------------------------------------
+// 4. suffix: one CTA per (chunk, b*h), thread = key dimension; r is replaced in place by
+//    its suffix sum over the sequence.
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kD) suffix_kernel(int L, int nc, float* dlg, const float* rtot) {
+  const int c = blockIdx.x, bh = blockIdx.y, i = threadIdx.x;
+  float carry = 0.f;
+  for (int c2 = nc - 1; c2 > c; --c2) carry += rtot[((size_t)bh * nc + c2) * kD + i];
+  const int t0 = c * kC, n = min(kC, L - t0);
+  float* r = dlg + ((size_t)bh * L + t0) * kD + i;
+  for (int tb = n; tb > 0; tb -= 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int tt = tb - 1 - u;
+      v[u] = tt >= 0 ? r[(size_t)tt * kD] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int tt = tb - 1 - u;
+      if (tt >= 0) {
+        carry += v[u];
+        r[(size_t)tt * kD] = carry;
+      }
+    }
+  }
+}
+
+template <typename K, typename M, typename P>
+cudaError_t launch_tc(K kernel, const M& maps, const P& p, int grid, int threads, size_t smem,
+                      const char* name, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  trace_begin(name, s);
+  kernel<<<grid, threads, smem, s>>>(maps, p);
+  trace_end(s);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_gla_tc_supported(int dk, int dv, int L, lizard_dtype dt) {
+  return dt == LIZARD_BF16 && dk == kD && dv == kD && L > 0 && tma_encode_available();
+}
+
+size_t bwd_gla_tc_workspace(int BH, int L) { return gla_ws_layout(BH, L, nullptr, nullptr); }
+
+cudaError_t launch_bwd_gla_tc(const BwdArgs& a, float* dvacc, unsigned char* ws, cudaStream_t s,
+                              int* launches) {
+  const int BH = a.B * a.H, L = a.L;
+  const int nc = (L + kC - 1) / kC;
+  GlaWs w;
+  gla_ws_layout(BH, L, ws, &w);
+  cudaError_t e;
+
+  PrepP pp{L, nc, static_cast<const bf16*>(a.pq), static_cast<const bf16*>(a.pk), a.lg, w, a.status};
+  trace_begin("bwd_prep", s);
+  prep_kernel<<<dim3(nc, BH), kD, 0, s>>>(pp);
+  trace_end(s);
+  ++*launches;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  const uint64_t bhl = (uint64_t)BH, Ll = (uint64_t)L, zs = (uint64_t)BH * nc;
+  ScanMaps sm;
+  bool ok = make_tma_map_bf16(&sm.x0, w.kt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&sm.y0, a.v, kD, Ll, bhl, kSl, kC, CU_TENSOR_MAP_SWIZZLE_64B) &&
+            make_tma_map_bf16(&sm.x1, w.qt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&sm.y1, a.dy, kD, Ll, bhl, kSl, kC, CU_TENSOR_MAP_SWIZZLE_64B);
+  ChunkMaps cm;
+  ok = ok && make_tma_map_bf16(&cm.dy, a.dy, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+       make_tma_map_bf16(&cm.v, a.v, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+       make_tma_map_bf16(&cm.qt, w.qt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+       make_tma_map_bf16(&cm.kt, w.kt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+       make_tma_map_bf16(&cm.hs, w.hs, kD, kD, zs, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+       make_tma_map_bf16(&cm.gs, w.gs, kD, kD, zs, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
+
+  ScanP sp{L, nc, a.h0, a.dh0, w, a.status};
+  e = launch_tc(scan_kernel, sm, sp, BH * kSlices * 2, kScanThreads, kScanSmem, "bwd_scan_tc", s);
+  ++*launches;
+  if (e != cudaSuccess) return e;
+
+  ChunkP cp{L, nc, w.eb, static_cast<bf16*>(a.dpq), static_cast<bf16*>(a.dpk), a.dlg, dvacc,
+            w.rtot, a.status};
+  e = launch_tc(chunk_kernel, cm, cp, BH * nc, kChunkThreads, kChunkSmem, "bwd_chunk_tc", s);
+  ++*launches;
+  if (e != cudaSuccess) return e;
+
+  trace_begin("bwd_suffix", s);
+  suffix_kernel<<<dim3(nc, BH), kD, 0, s>>>(L, nc, a.dlg, w.rtot);
+  trace_end(s);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+}  // namespace lz

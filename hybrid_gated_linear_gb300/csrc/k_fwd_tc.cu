@@ -652,9 +652,12 @@ fwd_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
   if (threadIdx.x == 0 && ctl->abort) raise_status(p.status, kDevTimeout);
 }
 
+}  // namespace
+
 // ------------------------------------------------------------------------------------
-// host side
+// host side: TMA descriptors
 // ------------------------------------------------------------------------------------
+namespace {
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -673,10 +676,12 @@ EncodeTiled get_encode() {
   });
   return fn;
 }
+}  // namespace
 
-// 3D bf16 map over [dim2][dim1][dim0] (dim0 contiguous) with a box {box0, box1, 1}.
-bool make_map(CUtensorMap* m, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
-              uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
+bool tma_encode_available() { return get_encode() != nullptr; }
+
+bool make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t dim0, uint64_t dim1,
+                       uint64_t dim2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
   EncodeTiled enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[3] = {dim0, dim1, dim2};
@@ -688,6 +693,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t dim0, uint64_t dim1, ui
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
 template <int NP>
 cudaError_t launch_np(const Maps& maps, const Params& p, int grid, cudaStream_t s) {
   const size_t smem = Cfg<NP>::TOTAL;
@@ -704,20 +710,20 @@ cudaError_t launch_np(const Maps& maps, const Params& p, int grid, cudaStream_t 
 
 bool fwd_tc_supported(const FwdArgs& a, lizard_dtype dt) {
   return dt == LIZARD_BF16 && a.dk == kD && a.dv == kD && a.L > 0 && a.W <= 2 * kC + 1 &&
-         a.M <= 16 && get_encode() != nullptr;
+         a.M <= 16 && tma_encode_available();
 }
 
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s, int* launches) {
   Maps maps;
   const uint64_t BH = (uint64_t)a.B * a.H, L = (uint64_t)a.L;
-  bool ok = make_map(&maps.phq, a.pq, kD, L, BH, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&maps.phk, a.pk, kD, L, BH, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&maps.q, a.q, kD, L, BH, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&maps.k, a.k, kD, L, BH, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&maps.v, a.v, kD, L, BH, kNV, kC, CU_TENSOR_MAP_SWIZZLE_64B);
+  bool ok = make_tma_map_bf16(&maps.phq, a.pq, kD, L, BH, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&maps.phk, a.pk, kD, L, BH, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&maps.q, a.q, kD, L, BH, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&maps.k, a.k, kD, L, BH, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&maps.v, a.v, kD, L, BH, kNV, kC, CU_TENSOR_MAP_SWIZZLE_64B);
   if (a.M > 0) {
-    ok = ok && make_map(&maps.mk, a.mk, kD, a.M, a.H, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         make_map(&maps.mv, a.mv, kD, a.M, a.H, kNV, 16, CU_TENSOR_MAP_SWIZZLE_64B);
+    ok = ok && make_tma_map_bf16(&maps.mk, a.mk, kD, a.M, a.H, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_tma_map_bf16(&maps.mv, a.mv, kD, a.M, a.H, kNV, 16, CU_TENSOR_MAP_SWIZZLE_64B);
   } else {
     maps.mk = maps.phq;
     maps.mv = maps.v;

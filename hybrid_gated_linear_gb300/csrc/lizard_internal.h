@@ -1,6 +1,7 @@
 // lizard_internal.h -- shared declarations of the CUDA library (not part of the ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -65,6 +66,13 @@ struct DecArgs {
 void trace_begin(const char* name, cudaStream_t s);
 void trace_end(cudaStream_t s);
 
+// TMA descriptors (driver entry point resolved once per process).
+bool tma_encode_available();
+// 3D bf16 tensor map over [dim2][dim1][dim0] (dim0 contiguous), box {box0, box1, 1}; rows
+// outside the tensor read as zeros.
+bool make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t dim0, uint64_t dim1,
+                       uint64_t dim2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw);
+
 // Launchers: return the first CUDA error and add the number of kernels they enqueued
 // to *launches.
 cudaError_t launch_chunk_cumsum(int units, int L, int dk, int chunk, const float* lg, float* b,
@@ -73,6 +81,13 @@ cudaError_t launch_fwd_simt(const FwdArgs& a, lizard_dtype dt, cudaStream_t s, i
 // Tensor-core forward (bf16, dk = dv = 128, W <= 129, M <= 16).
 bool fwd_tc_supported(const FwdArgs& a, lizard_dtype dt);
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s, int* launches);
+// Tensor-core backward of the GLA branch (bf16, dk = dv = 128, L > 0): writes d_phi_q,
+// d_phi_k, d_log_gamma, d_h0 and the GLA part of dv (fp32 [B*H][L][128]) to dvacc, using
+// bwd_gla_tc_workspace(B*H, L) bytes of scratch at ws (256-byte aligned).
+bool bwd_gla_tc_supported(int dk, int dv, int L, lizard_dtype dt);
+size_t bwd_gla_tc_workspace(int BH, int L);
+cudaError_t launch_bwd_gla_tc(const BwdArgs& a, float* dvacc, unsigned char* ws, cudaStream_t s,
+                              int* launches);
 size_t bwd_simt_workspace(int B, int H, int L, int dk, int dv, int M);
 cudaError_t launch_bwd_simt(const BwdArgs& a, lizard_dtype dt, cudaStream_t s, int* launches);
 cudaError_t launch_decode(const DecArgs& a, lizard_dtype dt, cudaStream_t s, int* launches);

@@ -25,6 +25,8 @@ def _check(g, ref, dtype, names=GRADS):
     (1, 1, 97, 128, 128, 8, 0.6, "bimodal"),   # W > L, M = 8
     (1, 2, 33, 64, 1, 0, 1.0, "plain"),        # W = 1, no meta
     (1, 1, 1, 128, 64, 2, 1.0, "plain"),       # one token
+    (1, 2, 640, 128, 64, 4, 1.0, "bimodal"),   # five whole 128-token chunks
+    (1, 1, 129, 128, 32, 4, 1.0, "slow"),      # one whole chunk and a one-token tail
 ])
 def test_bwd_matches_oracle(dtype, B, H, L, d, W, M, alpha, gate):
     x = synth.make_fwd_inputs(B, H, L, d, d, M, dtype, gate, seed=200 + L + W, with_dy=True)
@@ -67,3 +69,23 @@ def test_training_workload_sampled_head():
         got = g[n][h:h + 1] if n.startswith("d_meta") else g[n][:, h:h + 1]
         errs[n] = rel_l2(got, ref[n])
     assert all(e <= TOL["bf16"] for e in errs.values()), errs
+
+
+def test_bwd_flags_gate_sums_out_of_range():
+    """A chunk whose log-gate sum leaves [-80, 80] cannot be factorised into e^{+-b}; the
+    bf16 d = 128 path reports LIZARD_ERR_DEVICE_CHECK instead of returning silently."""
+    import torch
+    import hybrid_gated_linear_gb300 as lz
+    from gpu_util import code, to_dev
+    x = synth.make_fwd_inputs(1, 1, 256, 128, 128, 4, "bf16", "plain", seed=24, with_dy=True)
+    x["log_gamma"] = np.full_like(x["log_gamma"], -1.0)
+    t = to_dev({n: x[n] for n in NAMES + ("dy",)}, "bf16")
+    dims = lz.lizard_dims(1, 1, 256, 128, 128, 4, code("bf16"), 0.0)
+    ws = torch.zeros(lz.lizard_bwd_workspace_bytes(dims, 64), dtype=torch.uint8, device="cuda")
+    out = [torch.empty(1, 1, 256, 128, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    dlg = torch.empty(1, 1, 256, 128, dtype=torch.float32, device="cuda")
+    dq = [torch.empty(1, 1, 256, 128, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    dm = [torch.empty(1, 4, 128, dtype=torch.float32, device="cuda") for _ in range(2)]
+    lz.lizard_attn_bwd(dims, *(t[n] for n in NAMES), 64, 1.0, None, t["dy"], out[0], out[1],
+                       out[2], dlg, dq[0], dq[1], dm[0], dm[1], None, ws)
+    assert lz.lizard_check_device_errors(ws) == 5
