@@ -38,6 +38,7 @@ struct BwdWs {
   float* ds_meta;  // [BH][L][M]
   float* p_meta;   // [BH][L][M]
   float* dmeta_part;  // [nsplit][H][M][DK+DV]
+  float* mpart;       // per-block meta partials of the tensor-core window path
   int nsplit;
 };
 
@@ -67,6 +68,7 @@ BwdWs carve(unsigned char* p, int B, int H, int L, int dk, int dv, int M, bool t
   w.p_meta = take(BH * (size_t)L * M);
   w.nsplit = bwd_nsplit(B, H, L);
   w.dmeta_part = take((size_t)w.nsplit * H * M * (dk + dv));
+  w.mpart = dk == 128 && dv == 128 ? take(bwd_win_tc_meta_floats((int)BH, L, M)) : nullptr;
   w.states = nullptr;
   w.gla_tc = nullptr;
   if (tc) w.gla_tc = p + off;
@@ -85,6 +87,7 @@ size_t carve_bytes(int B, int H, int L, int dk, int dv, int M) {
   take(BH * (size_t)L * M);
   take(BH * (size_t)L * M);
   take((size_t)bwd_nsplit(B, H, L) * H * M * (dk + dv));
+  if (dk == 128 && dv == 128) take(bwd_win_tc_meta_floats((int)BH, L, M));
   const size_t simt = align_up(BH * nc * dk * dv * sizeof(float) + 1, 256);
   const size_t tc = dk == 128 && dv == 128 && L > 0 ? bwd_gla_tc_workspace((int)BH, L) : 0;
   return off + (simt > tc ? simt : tc);
@@ -565,6 +568,8 @@ cudaError_t launch_typed(const BwdArgs& a, cudaStream_t s, int* launches) {
     ++*launches;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  if (bwd_win_tc_supported(D, D, a.L, a.W, a.M, kDt))
+    return launch_bwd_win_tc(a, w.dvacc, w.lse, w.Dw, w.mpart, s, launches);
   if (a.L > 0) {
     const int zcap = a.M + a.W + 1;
     const size_t smem = (size_t)kWarps * (2 * D + zcap) * sizeof(float);

@@ -1,0 +1,635 @@
+// k_win_bwd_tc.cu -- backward of the anchor-window branch on tcgen05 tensor cores
+// (bf16, d = 128, W <= 65, M <= 16).
+//
+// Query i attends to the M meta keys and to keys j in [max(0, i-W+1), i] with
+// p_ij = softmax_j(scale q_i . k_j) (papernotes.org note on Lizard, 关键设计: Anchor Window
+// Attention); its output enters y with weight alpha, so dyw = alpha dy.  The pages give no
+// backward; the textbook softmax adjoint is
+//   dp_ij = dyw_i . v_j,  D_i = sum_j p_ij dp_ij,  ds_ij = p_ij (dp_ij - D_i)
+//   dq_i = scale sum_j ds_ij k_j,  dk_j = scale sum_i ds_ij q_i,  dv_j = sum_i p_ij dyw_i
+// and the meta keys/values collect the same sums over every query of the batch.
+//
+// Both kernels work on 128-token blocks; with W <= 65 a block of queries sees the keys
+// of the 192-row band [i0 - 64, i0 + 128), and a block of keys is seen by the queries of
+// the band [j0, j0 + 192).
+//   query kernel, per (b, h, queries i0 .. i0+127):
+//     Z  = Q [Km ; Kband]^T,  dP = dY [Vm ; Vband]^T       M=128 N=16+192 K=128
+//     per row: lse, D and ds (bf16, written over the V band in shared memory)
+//     dQ = ds [Km ; Kband]                                 M=128 N=128 K=16+192
+//     dMk^T = Q^T ds_meta,  dMv^T = dY^T p_meta            M=128 N=16  K=128
+//   key kernel, per (b, h, keys j0 .. j0+127):
+//     S^T = K Qband^T,  dP^T = V dYband^T                  M=128 N=192 K=128
+//     p, ds from S^T, dP^T and the query rows' lse and D
+//     dV = p^T dYband,  dK = ds^T Qband                    M=128 N=128 K=192
+//   meta kernel: ordered sum of the per-block meta partials over batch and blocks.
+// Every wait is bounded as in the other tensor-core kernels.
+#include "lizard_dev.cuh"
+#include "lizard_internal.h"
+#include "tc_sm100.cuh"
+
+namespace lz {
+namespace {
+
+using namespace tc;
+
+constexpr int kB = 128;   // block of queries / keys
+constexpr int kD = 128;   // dk = dv
+constexpr int kBand = 192;
+constexpr int kMetaRows = 16;
+constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr long long kWaitCycles = 2000000000ll;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kThreads = 6 * 32;  // warp 0 TMA, warp 1 MMA, warps 2-5 rows
+
+struct Ctl {
+  uint64_t bar[8];
+  uint32_t tmem;
+  int abort;
+};
+
+__device__ __forceinline__ bool wait_bar(Ctl* ctl, int i, uint32_t parity) {
+  uint64_t* b = &ctl->bar[i];
+  if (mbar_try_wait(b, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+#pragma unroll 1
+    for (int k = 0; k < 32; ++k)
+      if (mbar_try_wait(b, parity)) return true;
+    if (*(volatile int*)&ctl->abort) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *(volatile int*)&ctl->abort = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void drain_bar(Ctl* ctl, int i, uint64_t t0) {
+  while (!mbar_try_wait(&ctl->bar[i], 0))
+    if (globaltimer_ns() - t0 > kWaitNs) break;
+}
+
+// K-major SW128 descriptor, k-step j, tile of `rows` rows stored as 64-column blocks.
+__device__ __forceinline__ uint64_t desc_k(uint32_t base, int rows, int j) {
+  return smem_desc(base + (uint32_t)((j * 16) >> 6) * (uint32_t)rows * 128u + (uint32_t)((j * 16) & 63) * 2u,
+                   16, 1024, kSw128);
+}
+
+// MN-major SW128 descriptor, k-step j, tile whose `rows` rows are the K index and whose
+// 128 columns (two 64-column blocks) are the M or N index.
+__device__ __forceinline__ uint64_t desc_mn(uint32_t base, int rows, int j) {
+  return smem_desc(base + (uint32_t)j * 2048u, (uint32_t)rows * 128u, 1024, kSw128);
+}
+
+__device__ __forceinline__ void store16_bf16(unsigned char* tile, int rows, int row, int col, const float (&v)[16]) {
+  uint32_t w[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+  *reinterpret_cast<uint4*>(tile + sw128_offset(row, col, rows)) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(tile + sw128_offset(row, col + 8, rows)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+__device__ __forceinline__ void zero16_bf16(unsigned char* tile, int rows, int row, int col) {
+  *reinterpret_cast<uint4*>(tile + sw128_offset(row, col, rows)) = make_uint4(0, 0, 0, 0);
+  *reinterpret_cast<uint4*>(tile + sw128_offset(row, col + 8, rows)) = make_uint4(0, 0, 0, 0);
+}
+
+struct Params {
+  int H, L, M, W, nq;
+  float scale, alpha;
+  float* lse2;      // [BH][L]  log2-domain log-sum-exp of each query row
+  float* Dw;        // [BH][L]
+  float* mpart;     // [BH][nq][M][256] meta partials (dk part, then dv part)
+  const float* dvacc;  // [BH][L][128] GLA part of dv
+  bf16 *dq, *dk, *dv;
+  unsigned* status;
+};
+
+// ------------------------------------------------------------------------------------
+// query kernel
+// ------------------------------------------------------------------------------------
+struct QMaps {
+  CUtensorMap q, dy, kb, vb, mk, mv;
+};
+
+enum { Q_LDK = 0, Q_LDV, Q_ZF, Q_DPF, Q_DS, Q_OUT, Q_DONE };
+constexpr uint32_t QS_Q = 0, QS_DY = 32768, QS_KB = 65536, QS_VB = QS_KB + 49152,
+                   QS_KM = QS_VB + 49152, QS_VM = QS_KM + 4096, QS_DSM = QS_VM + 4096,
+                   QS_PM = QS_DSM + 4096, QS_BARS = QS_PM + 4096;
+constexpr size_t kQSmem = QS_BARS + 1024 + 1024;
+// TMEM columns: Z 0..207, dP 208..415, dMk 416, dMv 432; dQ reuses 0..127.
+constexpr uint32_t TQ_Z = 0, TQ_DP = 208, TQ_MK = 416, TQ_MV = 432, TQ_DQ = 0;
+
+__global__ void __launch_bounds__(kThreads, 1)
+win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Ctl* ctl = reinterpret_cast<Ctl*>(sm + QS_BARS);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qb = blockIdx.x % p.nq, bh = blockIdx.x / p.nq;
+  const int hh = bh % p.H;
+  const int L = p.L, M = p.M, W = p.W;
+  const int i0 = qb * kB;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i <= Q_DONE; ++i) mbar_init(&ctl->bar[i], i == Q_DS ? 128u : 1u);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint32_t meta_bytes = M > 0 ? 2u * kMetaRows * 128u : 0u;
+      mbar_arrive_expect_tx(&ctl->bar[Q_LDK], 32768 + 49152 + meta_bytes);
+      tma_load_3d(sm + QS_Q, &maps.q, 0, i0, bh, &ctl->bar[Q_LDK]);
+      tma_load_3d(sm + QS_Q + 16384, &maps.q, 64, i0, bh, &ctl->bar[Q_LDK]);
+      tma_load_3d(sm + QS_KB, &maps.kb, 0, i0 - 64, bh, &ctl->bar[Q_LDK]);
+      tma_load_3d(sm + QS_KB + 24576, &maps.kb, 64, i0 - 64, bh, &ctl->bar[Q_LDK]);
+      if (M > 0) {
+        tma_load_3d(sm + QS_KM, &maps.mk, 0, 0, hh, &ctl->bar[Q_LDK]);
+        tma_load_3d(sm + QS_KM + 2048, &maps.mk, 64, 0, hh, &ctl->bar[Q_LDK]);
+      }
+      mbar_arrive_expect_tx(&ctl->bar[Q_LDV], 32768 + 49152 + meta_bytes);
+      tma_load_3d(sm + QS_DY, &maps.dy, 0, i0, bh, &ctl->bar[Q_LDV]);
+      tma_load_3d(sm + QS_DY + 16384, &maps.dy, 64, i0, bh, &ctl->bar[Q_LDV]);
+      tma_load_3d(sm + QS_VB, &maps.vb, 0, i0 - 64, bh, &ctl->bar[Q_LDV]);
+      tma_load_3d(sm + QS_VB + 24576, &maps.vb, 64, i0 - 64, bh, &ctl->bar[Q_LDV]);
+      if (M > 0) {
+        tma_load_3d(sm + QS_VM, &maps.mv, 0, 0, hh, &ctl->bar[Q_LDV]);
+        tma_load_3d(sm + QS_VM + 2048, &maps.mv, 64, 0, hh, &ctl->bar[Q_LDV]);
+      }
+      const uint64_t tw = globaltimer_ns();
+      drain_bar(ctl, Q_LDK, tw);
+      drain_bar(ctl, Q_LDV, tw);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t sb = smem_u32(sm);
+      const uint32_t id16 = idesc_bf16(kB, kMetaRows, false, false);
+      const uint32_t id192 = idesc_bf16(kB, kBand, false, false);
+      const uint32_t id_dq = idesc_bf16(kB, kD, false, true);
+      const uint32_t id_dqm = idesc_bf16(kB, kD, true, true);
+      const uint32_t id_meta = idesc_bf16(kD, kMetaRows, true, false);
+      bool ok = wait_bar(ctl, Q_LDK, 0);
+      if (ok) {
+        tc_fence_after();
+        if (M > 0)
+          for (int j = 0; j < 8; ++j)
+            mma_bf16(tmem + TQ_Z, desc_k(sb + QS_Q, kB, j), desc_k(sb + QS_KM, kMetaRows, j), id16, j > 0);
+        for (int j = 0; j < 8; ++j)
+          mma_bf16(tmem + TQ_Z + 16, desc_k(sb + QS_Q, kB, j), desc_k(sb + QS_KB, kBand, j), id192, j > 0);
+        mma_commit(&ctl->bar[Q_ZF]);
+      }
+      if (ok && (ok = wait_bar(ctl, Q_LDV, 0))) {
+        tc_fence_after();
+        if (M > 0)
+          for (int j = 0; j < 8; ++j)
+            mma_bf16(tmem + TQ_DP, desc_k(sb + QS_DY, kB, j), desc_k(sb + QS_VM, kMetaRows, j), id16, j > 0);
+        for (int j = 0; j < 8; ++j)
+          mma_bf16(tmem + TQ_DP + 16, desc_k(sb + QS_DY, kB, j), desc_k(sb + QS_VB, kBand, j), id192, j > 0);
+        mma_commit(&ctl->bar[Q_DPF]);
+      }
+      if (ok && (ok = wait_bar(ctl, Q_DS, 0))) {
+        tc_fence_after();
+        // dQ = ds_band Kband (+ ds_meta Km); ds_band lives over the V band
+        for (int j = 0; j < kBand / 16; ++j)
+          mma_bf16(tmem + TQ_DQ, desc_k(sb + QS_VB, kB, j), desc_mn(sb + QS_KB, kBand, j), id_dq, j > 0);
+        if (M > 0) {
+          mma_bf16(tmem + TQ_DQ, smem_desc(sb + QS_DSM, kMetaRows * 128u, 1024, kSw128),
+                   smem_desc(sb + QS_KM, kMetaRows * 128u, 1024, kSw128), id_dqm, true);
+          for (int j = 0; j < 8; ++j)
+            mma_bf16(tmem + TQ_MK, desc_mn(sb + QS_Q, kB, j), desc_k(sb + QS_DSM, kMetaRows, j), id_meta, j > 0);
+          for (int j = 0; j < 8; ++j)
+            mma_bf16(tmem + TQ_MV, desc_mn(sb + QS_DY, kB, j), desc_k(sb + QS_PM, kMetaRows, j), id_meta, j > 0);
+        }
+        mma_commit(&ctl->bar[Q_OUT]);
+      }
+      if (!ok) ctl->abort = 1;
+      mma_commit(&ctl->bar[Q_DONE]);
+      drain_bar(ctl, Q_DONE, globaltimer_ns());
+    }
+  } else {
+    const int qw = warp & 3;
+    const int r = qw * 32 + lane;  // query row of the block
+    const int i = i0 + r;
+    const bool valid = i < L;
+    const uint32_t tl = tmem + ((uint32_t)(qw * 32) << 16);
+    const float zs = p.scale * kLog2e;
+    // band columns b <-> key j = i0 - 64 + b; this row sees b in [blo, bhi]
+    const int bhi = 64 + r;
+    const int blo = max(64 + r - W + 1, 64 - i0);
+    // 16-column band groups any row of this warp can see
+    const int g_lo = max(0, 64 + 32 * qw - W + 1) >> 4;
+    const int g_hi = (64 + 32 * qw + 31) >> 4;
+    const int nmeta = M > 0 ? 1 : 0;
+    const int ng = nmeta + g_hi - g_lo + 1;
+    auto zcol = [&](int g) { return g < nmeta ? 0 : 16 + 16 * (g_lo + g - nmeta); };
+    auto vis = [&](int g, int e) {
+      if (g < nmeta) return e < M;
+      const int b = 16 * (g_lo + g - nmeta) + e;
+      return b >= blo && b <= bhi;
+    };
+    bool ok = wait_bar(ctl, Q_ZF, 0);
+    float mx = -INFINITY;
+    if (ok) {
+      tc_fence_after();
+      for (int g = 0; g < ng; ++g) {
+        uint32_t z[16];
+        tmem_ld16(tl + TQ_Z + zcol(g), z);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          if (vis(g, e)) mx = fmaxf(mx, __uint_as_float(z[e]));
+      }
+    }
+    const float mxs = mx * zs;
+    float sum = 0.f, sdp = 0.f;
+    if (ok && (ok = wait_bar(ctl, Q_DPF, 0))) {
+      tc_fence_after();
+      for (int g = 0; g < ng; ++g) {
+        uint32_t z[16], d[16];
+        tmem_ld16(tl + TQ_Z + zcol(g), z);
+        tmem_ld16(tl + TQ_DP + zcol(g), d);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float ex = vis(g, e) ? ex2_approx(fmaf(__uint_as_float(z[e]), zs, -mxs)) : 0.f;
+          sum += ex;
+          sdp = fmaf(ex, __uint_as_float(d[e]), sdp);
+        }
+      }
+    }
+    const float lse2 = mxs + __log2f(sum);
+    const float Dv = p.alpha * sdp / sum;
+    unsigned char* dsb = sm + QS_VB;  // ds band tile, 128 rows x 192 columns
+    if (ok) {
+      for (int g = 0; g < ng; ++g) {
+        uint32_t z[16], d[16];
+        tmem_ld16(tl + TQ_Z + zcol(g), z);
+        tmem_ld16(tl + TQ_DP + zcol(g), d);
+        tmem_ld_wait();
+        float ds[16], pp[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float pe = (valid && vis(g, e)) ? ex2_approx(fmaf(__uint_as_float(z[e]), zs, -lse2)) : 0.f;
+          pp[e] = pe;
+          ds[e] = pe * fmaf(p.alpha, __uint_as_float(d[e]), -Dv);
+        }
+        if (g < nmeta) {
+          // transposed meta tiles: row m, column r
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            *reinterpret_cast<bf16*>(sm + QS_DSM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(ds[e]);
+            *reinterpret_cast<bf16*>(sm + QS_PM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(pp[e]);
+          }
+        } else {
+          store16_bf16(dsb, kB, r, 16 * (g_lo + g - nmeta), ds);
+        }
+      }
+    }
+    // band groups no row of this warp sees hold zeros (the tile still holds V)
+    for (int g = 0; g < kBand / 16; ++g)
+      if (g < g_lo || g > g_hi) zero16_bf16(dsb, kB, r, 16 * g);
+    if (M == 0) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        *reinterpret_cast<bf16*>(sm + QS_DSM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(0.f);
+        *reinterpret_cast<bf16*>(sm + QS_PM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(0.f);
+      }
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();
+    mbar_arrive(&ctl->bar[Q_DS]);
+    if (ok && valid) {
+      p.lse2[(size_t)bh * L + i] = lse2;
+      p.Dw[(size_t)bh * L + i] = Dv;
+    }
+    if (ok && (ok = wait_bar(ctl, Q_OUT, 0))) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < kD; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tl + TQ_DQ + c, v);
+        tmem_ld_wait();
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dq + ((size_t)bh * L + i) * kD + c);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16x2(p.scale * __uint_as_float(v[8 * m + 2 * e]),
+                                 p.scale * __uint_as_float(v[8 * m + 2 * e + 1]));
+            dst[m] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      if (M > 0) {
+        // lane r of the meta products = feature dimension r
+        uint32_t mk[16], mv[16];
+        tmem_ld16(tl + TQ_MK, mk);
+        tmem_ld16(tl + TQ_MV, mv);
+        tmem_ld_wait();
+        float* part = p.mpart + ((size_t)bh * p.nq + qb) * M * 256;
+#pragma unroll
+        for (int m = 0; m < kMetaRows; ++m) {
+          if (m < M) {
+            part[m * 256 + r] = __uint_as_float(mk[m]);
+            part[m * 256 + 128 + r] = __uint_as_float(mv[m]);
+          }
+        }
+      }
+    }
+    if (!ok) ctl->abort = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && ctl->abort) raise_status(p.status, kDevTimeout);
+}
+
+// ------------------------------------------------------------------------------------
+// key kernel
+// ------------------------------------------------------------------------------------
+struct KMaps {
+  CUtensorMap k, v, qb, dyb;
+};
+
+enum { K_LDK = 0, K_LDV, K_SF, K_PDS, K_OUT, K_DONE };
+constexpr uint32_t KS_K = 0, KS_V = 32768, KS_PT = 0 /* over K and V */, KS_QB = 65536,
+                   KS_DYB = KS_QB + 49152, KS_DST = KS_DYB + 49152, KS_ROW = KS_DST + 49152,
+                   KS_BARS = KS_ROW + 2048;
+constexpr size_t kKSmem = KS_BARS + 1024 + 1024;
+constexpr uint32_t TK_S = 0, TK_DP = 192, TK_DV = 0, TK_DK = 192;
+
+__global__ void __launch_bounds__(kThreads, 1)
+win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Ctl* ctl = reinterpret_cast<Ctl*>(sm + KS_BARS);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kb = blockIdx.x % p.nq, bh = blockIdx.x / p.nq;
+  const int L = p.L, W = p.W;
+  const int j0 = kb * kB;
+  float* rl = reinterpret_cast<float*>(sm + KS_ROW);  // lse2 of the band's query rows
+  float* rd = rl + kBand;                             // D of the band's query rows
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i <= K_DONE; ++i) mbar_init(&ctl->bar[i], i == K_PDS ? 128u : 1u);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&ctl->bar[K_LDK], 32768 + 49152);
+      tma_load_3d(sm + KS_K, &maps.k, 0, j0, bh, &ctl->bar[K_LDK]);
+      tma_load_3d(sm + KS_K + 16384, &maps.k, 64, j0, bh, &ctl->bar[K_LDK]);
+      tma_load_3d(sm + KS_QB, &maps.qb, 0, j0, bh, &ctl->bar[K_LDK]);
+      tma_load_3d(sm + KS_QB + 24576, &maps.qb, 64, j0, bh, &ctl->bar[K_LDK]);
+      mbar_arrive_expect_tx(&ctl->bar[K_LDV], 32768 + 49152);
+      tma_load_3d(sm + KS_V, &maps.v, 0, j0, bh, &ctl->bar[K_LDV]);
+      tma_load_3d(sm + KS_V + 16384, &maps.v, 64, j0, bh, &ctl->bar[K_LDV]);
+      tma_load_3d(sm + KS_DYB, &maps.dyb, 0, j0, bh, &ctl->bar[K_LDV]);
+      tma_load_3d(sm + KS_DYB + 24576, &maps.dyb, 64, j0, bh, &ctl->bar[K_LDV]);
+      const uint64_t tw = globaltimer_ns();
+      drain_bar(ctl, K_LDK, tw);
+      drain_bar(ctl, K_LDV, tw);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t sb = smem_u32(sm);
+      const uint32_t id_s = idesc_bf16(kB, kBand, false, false);
+      const uint32_t id_o = idesc_bf16(kB, kD, false, true);
+      bool ok = wait_bar(ctl, K_LDK, 0);
+      if (ok) {
+        tc_fence_after();
+        for (int j = 0; j < 8; ++j)
+          mma_bf16(tmem + TK_S, desc_k(sb + KS_K, kB, j), desc_k(sb + KS_QB, kBand, j), id_s, j > 0);
+      }
+      if (ok && (ok = wait_bar(ctl, K_LDV, 0))) {
+        tc_fence_after();
+        for (int j = 0; j < 8; ++j)
+          mma_bf16(tmem + TK_DP, desc_k(sb + KS_V, kB, j), desc_k(sb + KS_DYB, kBand, j), id_s, j > 0);
+        mma_commit(&ctl->bar[K_SF]);
+      }
+      if (ok && (ok = wait_bar(ctl, K_PDS, 0))) {
+        tc_fence_after();
+        for (int j = 0; j < kBand / 16; ++j)
+          mma_bf16(tmem + TK_DV, desc_k(sb + KS_PT, kB, j), desc_mn(sb + KS_DYB, kBand, j), id_o, j > 0);
+        for (int j = 0; j < kBand / 16; ++j)
+          mma_bf16(tmem + TK_DK, desc_k(sb + KS_DST, kB, j), desc_mn(sb + KS_QB, kBand, j), id_o, j > 0);
+        mma_commit(&ctl->bar[K_OUT]);
+      }
+      if (!ok) ctl->abort = 1;
+      mma_commit(&ctl->bar[K_DONE]);
+      drain_bar(ctl, K_DONE, globaltimer_ns());
+    }
+  } else {
+    const int qw = warp & 3;
+    const int jr = qw * 32 + lane;  // key row of the block
+    const int j = j0 + jr;
+    const bool valid = j < L;
+    const uint32_t tl = tmem + ((uint32_t)(qw * 32) << 16);
+    const float zs = p.scale * kLog2e;
+    const int et = threadIdx.x - 64;  // 0..127
+    for (int u = et; u < kBand; u += 128) {
+      const int i = j0 + u;
+      rl[u] = i < L ? p.lse2[(size_t)bh * L + i] : INFINITY;
+      rd[u] = i < L ? p.Dw[(size_t)bh * L + i] : 0.f;
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    // query column u <-> query i = j0 + u; this row is seen by u in [jr, jr + W - 1]
+    const int g_lo = (32 * qw) >> 4;
+    const int g_hi = min(kBand - 1, 32 * qw + 31 + W - 1) >> 4;
+    unsigned char* pt = sm + KS_PT;
+    unsigned char* dst = sm + KS_DST;
+    bool ok = wait_bar(ctl, K_SF, 0);
+    if (ok) {
+      tc_fence_after();
+      for (int g = g_lo; g <= g_hi; ++g) {
+        uint32_t s[16], d[16];
+        tmem_ld16(tl + TK_S + 16 * g, s);
+        tmem_ld16(tl + TK_DP + 16 * g, d);
+        tmem_ld_wait();
+        float pp[16], ds[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int u = 16 * g + e;
+          const bool vis = valid && u >= jr && u <= jr + W - 1;
+          const float pe = vis ? ex2_approx(fmaf(__uint_as_float(s[e]), zs, -rl[u])) : 0.f;
+          pp[e] = pe;
+          ds[e] = pe * fmaf(p.alpha, __uint_as_float(d[e]), -rd[u]);
+        }
+        store16_bf16(pt, kB, jr, 16 * g, pp);
+        store16_bf16(dst, kB, jr, 16 * g, ds);
+      }
+    }
+    for (int g = 0; g < kBand / 16; ++g) {
+      if (g < g_lo || g > g_hi) {
+        zero16_bf16(pt, kB, jr, 16 * g);
+        zero16_bf16(dst, kB, jr, 16 * g);
+      }
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();
+    mbar_arrive(&ctl->bar[K_PDS]);
+    if (ok && (ok = wait_bar(ctl, K_OUT, 0))) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < kD; c += 32) {
+        uint32_t v[32], k[32];
+        tmem_ld32(tl + TK_DV + c, v);
+        tmem_ld32(tl + TK_DK + c, k);
+        tmem_ld_wait();
+        if (valid) {
+          const size_t row = ((size_t)bh * L + j) * kD + c;
+          const float4* ga = reinterpret_cast<const float4*>(p.dvacc + row);
+          uint4* dvo = reinterpret_cast<uint4*>(p.dv + row);
+          uint4* dko = reinterpret_cast<uint4*>(p.dk + row);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float4 a0 = ga[2 * m], a1 = ga[2 * m + 1];
+            const float gv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            uint32_t wv[4], wk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              wv[e] = pack_bf16x2(fmaf(p.alpha, __uint_as_float(v[8 * m + 2 * e]), gv[2 * e]),
+                                  fmaf(p.alpha, __uint_as_float(v[8 * m + 2 * e + 1]), gv[2 * e + 1]));
+              wk[e] = pack_bf16x2(p.scale * __uint_as_float(k[8 * m + 2 * e]),
+                                  p.scale * __uint_as_float(k[8 * m + 2 * e + 1]));
+            }
+            dvo[m] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            dko[m] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+          }
+        }
+      }
+    }
+    if (!ok) ctl->abort = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && ctl->abort) raise_status(p.status, kDevTimeout);
+}
+
+// ------------------------------------------------------------------------------------
+// meta gradients: ordered sum of the per-block partials over (batch, block).
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) win_meta_kernel(int B, int H, int M, int nq, float scale,
+                                                       float alpha, const float* mpart, float* dmk,
+                                                       float* dmv) {
+  const int hh = blockIdx.x, m = blockIdx.y, d = threadIdx.x;
+  float s = 0.f;
+  for (int b = 0; b < B; ++b) {
+    const float* part = mpart + ((size_t)(b * H + hh) * nq) * M * 256 + m * 256 + d;
+    for (int q = 0; q < nq; ++q) s += part[(size_t)q * M * 256];
+  }
+  if (d < kD) dmk[((size_t)hh * M + m) * kD + d] = scale * s;
+  else dmv[((size_t)hh * M + m) * kD + d - kD] = alpha * s;
+}
+
+template <typename K, typename Mp>
+cudaError_t launch_tc(K kernel, const Mp& maps, const Params& p, int grid, size_t smem,
+                      const char* name, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  trace_begin(name, s);
+  kernel<<<grid, kThreads, smem, s>>>(maps, p);
+  trace_end(s);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_win_tc_supported(int dk, int dv, int L, int W, int M, lizard_dtype dt) {
+  return dt == LIZARD_BF16 && dk == kD && dv == kD && L > 0 && W >= 1 && W <= 65 &&
+         M <= kMetaRows && tma_encode_available();
+}
+
+size_t bwd_win_tc_meta_floats(int BH, int L, int M) {
+  return (size_t)BH * ((L + kB - 1) / kB) * M * 256;
+}
+
+cudaError_t launch_bwd_win_tc(const BwdArgs& a, const float* dvacc, float* lse2, float* Dw,
+                              float* mpart, cudaStream_t s, int* launches) {
+  const int BH = a.B * a.H, L = a.L;
+  const int nq = (L + kB - 1) / kB;
+  const uint64_t bhl = (uint64_t)BH, Ll = (uint64_t)L;
+  QMaps qm;
+  KMaps km;
+  bool ok = make_tma_map_bf16(&qm.q, a.q, kD, Ll, bhl, 64, kB, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&qm.dy, a.dy, kD, Ll, bhl, 64, kB, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&qm.kb, a.k, kD, Ll, bhl, 64, kBand, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&qm.vb, a.v, kD, Ll, bhl, 64, kBand, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&km.k, a.k, kD, Ll, bhl, 64, kB, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&km.v, a.v, kD, Ll, bhl, 64, kB, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&km.qb, a.q, kD, Ll, bhl, 64, kBand, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&km.dyb, a.dy, kD, Ll, bhl, 64, kBand, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (a.M > 0) {
+    ok = ok && make_tma_map_bf16(&qm.mk, a.mk, kD, a.M, a.H, 64, kMetaRows, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_tma_map_bf16(&qm.mv, a.mv, kD, a.M, a.H, 64, kMetaRows, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    qm.mk = qm.q;
+    qm.mv = qm.dy;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  Params p;
+  p.H = a.H;
+  p.L = L;
+  p.M = a.M;
+  p.W = a.W;
+  p.nq = nq;
+  p.scale = a.scale;
+  p.alpha = a.alpha;
+  p.lse2 = lse2;
+  p.Dw = Dw;
+  p.mpart = mpart;
+  p.dvacc = dvacc;
+  p.dq = static_cast<bf16*>(a.dq);
+  p.dk = static_cast<bf16*>(a.dk_);
+  p.dv = static_cast<bf16*>(a.dvv);
+  p.status = a.status;
+  cudaError_t e = launch_tc(win_q_kernel, qm, p, BH * nq, kQSmem, "win_bwd_q_tc", s);
+  ++*launches;
+  if (e != cudaSuccess) return e;
+  e = launch_tc(win_k_kernel, km, p, BH * nq, kKSmem, "win_bwd_k_tc", s);
+  ++*launches;
+  if (e != cudaSuccess) return e;
+  if (a.M > 0) {
+    trace_begin("win_bwd_meta", s);
+    win_meta_kernel<<<dim3(a.H, a.M), 256, 0, s>>>(a.B, a.H, a.M, nq, a.scale, a.alpha, mpart,
+                                                    a.dmk, a.dmv);
+    trace_end(s);
+    ++*launches;
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace lz

@@ -88,6 +88,13 @@ bool bwd_gla_tc_supported(int dk, int dv, int L, lizard_dtype dt);
 size_t bwd_gla_tc_workspace(int BH, int L);
 cudaError_t launch_bwd_gla_tc(const BwdArgs& a, float* dvacc, unsigned char* ws, cudaStream_t s,
                               int* launches);
+// Tensor-core backward of the window branch (bf16, dk = dv = 128, 1 <= W <= 65, M <= 16,
+// L > 0): writes d_q, d_k, d_v (adding the GLA part from dvacc), d_meta_k, d_meta_v; uses
+// lse2/Dw ([B*H][L] fp32) and mpart (bwd_win_tc_meta_floats) as scratch.
+bool bwd_win_tc_supported(int dk, int dv, int L, int W, int M, lizard_dtype dt);
+size_t bwd_win_tc_meta_floats(int BH, int L, int M);
+cudaError_t launch_bwd_win_tc(const BwdArgs& a, const float* dvacc, float* lse2, float* Dw,
+                              float* mpart, cudaStream_t s, int* launches);
 size_t bwd_simt_workspace(int B, int H, int L, int dk, int dv, int M);
 cudaError_t launch_bwd_simt(const BwdArgs& a, lizard_dtype dt, cudaStream_t s, int* launches);
 cudaError_t launch_decode(const DecArgs& a, lizard_dtype dt, cudaStream_t s, int* launches);
