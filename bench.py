@@ -16,6 +16,7 @@ same workload and prints the same kind of line.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -36,11 +37,39 @@ NAMES = ("phi_q", "phi_k", "v", "log_gamma", "q", "k", "meta_k", "meta_v")
 # Algorithmic HBM bytes per (token, head) of each kernel at d = 128 (bf16 tensors, fp32
 # log gamma): what the kernel must read and write at minimum.
 ALGO_BYTES_PER_TOKEN_HEAD = {
-    "fwd_simt": 5 * 256 + 512 + 256,          # phi_q, phi_k, v, q, k + log_gamma + y
-    "gla_bwd_simt": 4 * 256 + 512 + 2 * 256 + 512,  # phi_q, phi_k, v, dy, lg; d_phi_q/k, d_lg
-    "win_bwd_query": 4 * 256 + 256,           # q, k, v, dy + d_q
-    "win_bwd_key": 4 * 256 + 2 * 256,         # q, k, v, dy + d_k, d_v
+    # bytes each kernel must move per (token, head) at d = 128: bf16 rows are 256 B,
+    # fp32 rows 512 B; per-chunk states are amortised over the chunk's tokens.
+    "fwd_tc": 5 * 256 + 512 + 256,            # phi_q, phi_k, v, q, k, log_gamma -> y
+    "fwd_simt": 5 * 256 + 512 + 256,
+    "bwd_prep": 2 * 256 + 512 + 3 * 256,      # phi_q, phi_k, log_gamma -> Qt, Kt, e^b
+    "bwd_scan_tc": 4 * 256 + 2 * 256,         # Qt, Kt, v, dy -> h, Gt (2 x 32 KB / 128 tokens)
+    "bwd_chunk_tc": 4 * 256 + 2 * 256 + 256 + 2 * 256 + 2 * 512,  # + e^b -> d_phi, dv_gla, r
+    "bwd_suffix": 2 * 512,                    # r -> d_log_gamma
+    "win_bwd_q_tc": 4 * 256 + 256 + 8,        # q, dy, k, v -> d_q, lse, D
+    "win_bwd_k_tc": 4 * 256 + 512 + 8 + 2 * 256,  # q, dy, k, v, dv_gla, lse, D -> d_k, d_v
+    "gla_bwd_simt": 4 * 256 + 512 + 2 * 256 + 512,
+    "win_bwd_query": 4 * 256 + 256,
+    "win_bwd_key": 4 * 256 + 2 * 256,
 }
+# DRAM bytes (read + write) per (token, head) from the ncu captures summarised under
+# profiles/, each with the sha256 of the kernel source it was taken on: a kernel whose
+# source changed since then reports "traffic": null.
+PROFILED_TRAFFIC = {
+    # profiles/ncu_step_kernels_llama3_8b.md
+    "fwd_tc": {"bytes_per_token_head": 1981, "source": "hybrid_gated_linear_gb300/csrc/k_fwd_tc.cu",
+               "sha256": "9e04ddd3da7ad346c79e63e8d7f9afdfc485d93d69748f68e7a4fcdd0afdb561"},
+    "bwd_prep": {"bytes_per_token_head": 1506, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
+                 "sha256": "f45c7cbee44dc30cee745e5d71dd6f87390fddc0727852b9a378a7caa2e47fcf"},
+    "bwd_scan_tc": {"bytes_per_token_head": 1277, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
+                    "sha256": "f45c7cbee44dc30cee745e5d71dd6f87390fddc0727852b9a378a7caa2e47fcf"},
+    "bwd_chunk_tc": {"bytes_per_token_head": 2961, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
+                     "sha256": "f45c7cbee44dc30cee745e5d71dd6f87390fddc0727852b9a378a7caa2e47fcf"},
+    "win_bwd_q_tc": {"bytes_per_token_head": 1167, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
+                     "sha256": "a5ea4645244a74af8f6e137ceee39f30a223edc2c2305b5f2d3f82e318bd1c41"},
+    "win_bwd_k_tc": {"bytes_per_token_head": 1874, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
+                     "sha256": "a5ea4645244a74af8f6e137ceee39f30a223edc2c2305b5f2d3f82e318bd1c41"},
+}
+
 DECODE_BYTES_PER_UNIT = 2 * 65536 + 2 * 64 * 128 * 2 + 5 * 256 + 512 + 2 * 256 + 256
 
 
@@ -56,16 +85,19 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while running."""
+    """nvidia-smi clock/throttle samples every 20 ms; summary() keeps the samples taken
+    while the timed region ran (between mark_start and mark_end, one interval of slack)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -73,11 +105,24 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+        # start timing only once the sampler is producing samples
+        deadline = time.time() + 5.0
+        while self.proc is not None and time.time() < deadline:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
         return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+        time.sleep(2 * self.INTERVAL_MS / 1000.0)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -87,12 +132,20 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
+    @staticmethod
+    def _when(stamp):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def summary(self):
         rows = []
         try:
             for line in open(self.path):
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
+                if len(parts) >= 10:
                     rows.append(parts)
         except Exception:
             pass
@@ -103,12 +156,19 @@ class ClockSampler:
                 pass
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        slack = self.INTERVAL_MS / 1000.0
+        inside = [r for r in rows
+                  if self.t0 is not None and self._when(r[0]) is not None
+                  and self.t0 - slack <= self._when(r[0]) <= self.t1 + slack]
+        use = inside if inside else rows
+        sm = [float(r[2]) for r in use if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in use if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        reasons = sorted({names[i] for r in use for i in range(4) if r[6 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "interval_ms": self.INTERVAL_MS,
+                "window": "timed region" if inside else "whole timing block (none inside)"}
 
 
 def _dist():
@@ -261,6 +321,19 @@ def _time_steps(fn, steps, flush, stream):
     return [a.elapsed_time(b) for a, b in times]
 
 
+def _profiled_traffic(kernel, units):
+    rec = PROFILED_TRAFFIC.get(kernel)
+    if rec is None:
+        return None
+    try:
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
+                return None
+    except OSError:
+        return None
+    return rec["bytes_per_token_head"] * units
+
+
 def _roofline_from_trace(trace, w, peaks, steps):
     """Dominant kernel over the timed steps -> roofline object."""
     tot, cnt = {}, {}
@@ -273,14 +346,22 @@ def _roofline_from_trace(trace, w, peaks, steps):
     units = w["B"] * w["H"] * w["L"]
     per_launch_ms = tot[dom] / cnt[dom]
     algo = ALGO_BYTES_PER_TOKEN_HEAD.get(dom)
-    kernels = {k: {"launches_per_step": cnt[k] / steps, "ms_per_launch": tot[k] / cnt[k],
-                   "share": tot[k] / sum(tot.values())} for k in tot}
+    kernels = {}
+    for k in tot:
+        ms_k = tot[k] / cnt[k]
+        kernels[k] = {"launches_per_step": cnt[k] / steps, "ms_per_launch": ms_k,
+                      "share": tot[k] / sum(tot.values())}
+        if k in ALGO_BYTES_PER_TOKEN_HEAD:
+            gbs = ALGO_BYTES_PER_TOKEN_HEAD[k] * units / (ms_k * 1e-3) / 1e9
+            kernels[k]["algorithmic_gbs"] = gbs
+            kernels[k]["hbm_frac"] = gbs / peaks["hbm_gbs"]
     if algo is None:
         return {"kernel": dom, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": None, "traffic": None}, kernels
     achieved = algo * units / (per_launch_ms * 1e-3) / 1e9
     return {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+            "traffic": _profiled_traffic(dom, units),
             "algorithmic_bytes_per_launch": algo * units,
             "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"}, kernels
 
@@ -381,7 +462,7 @@ def _e2e(prob, x, steps, dev):
     return a.elapsed_time(b) / steps, h2d, d2h
 
 
-def _cpu_baseline(w, budget_s=20.0):
+def _cpu_baseline(w, budget_s=10.0):
     import oracle
     import synth
     cores = os.cpu_count() or 1
@@ -389,14 +470,20 @@ def _cpu_baseline(w, budget_s=20.0):
     x = synth.make_fwd_inputs(1, heads, w["L"], w["dk"], w["dv"], w["M"], "bf16", w["gate"],
                               seed=w["seed"], with_dy=True)
     oracle.build()
+    reps = 0
     t0 = time.perf_counter()
-    oracle.fwd(*(x[n] for n in NAMES), W=w["W"], nthreads=heads)
-    oracle.bwd(*(x[n] for n in NAMES), x["dy"], W=w["W"], nthreads=heads)
-    dt = time.perf_counter() - t0
-    return {"value": w["L"] * heads / w["H"] / dt, "unit": "tokens/s",
+    while True:
+        oracle.fwd(*(x[n] for n in NAMES), W=w["W"], nthreads=heads)
+        oracle.bwd(*(x[n] for n in NAMES), x["dy"], W=w["W"], nthreads=heads)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s:
+            break
+    return {"value": reps * w["L"] * heads / w["H"] / dt, "unit": "tokens/s",
             "cores": oracle.last_threads(), "kind": "oracle",
-            "sample": f"one fwd+bwd of {heads} of {w['H']} heads at L={w['L']}, d={w['dk']} "
-                      f"({dt:.1f} s wall, fp64 C oracle, one thread per head)"}
+            "sample": f"{reps} fwd+bwd passes over {heads} of {w['H']} heads at L={w['L']}, "
+                      f"d={w['dk']} ({dt:.1f} s wall, fp64 C oracle, one thread per head); "
+                      "tokens/s scaled to all heads"}
 
 
 def run_ours(args):
@@ -433,7 +520,9 @@ def run_ours(args):
         torch.cuda.synchronize()
         prob.launches = 0
         lz.lizard_trace_enable(True)
+        clk.mark_start()
         times = _time_steps(prob.step, args.steps, flush, stream)
+        clk.mark_end()
         lz.lizard_trace_enable(False)
         trace = lz.lizard_trace_read()
         torch.cuda.synchronize()
