@@ -39,7 +39,9 @@ NAMES = ("phi_q", "phi_k", "v", "log_gamma", "q", "k", "meta_k", "meta_v")
 ALGO_BYTES_PER_TOKEN_HEAD = {
     # bytes each kernel must move per (token, head) at d = 128: bf16 rows are 256 B,
     # fp32 rows 512 B; per-chunk states are amortised over the chunk's tokens.
-    "fwd_tc": 5 * 256 + 512 + 256,            # phi_q, phi_k, v, q, k, log_gamma -> y
+    "fwd_prep": 2 * 256 + 512 + 2 * 256,      # phi_q, phi_k, log_gamma -> Qt, Kt
+    "fwd_scan_tc": 2 * 256 + 256,             # Kt, v -> h (32 KB per 128-token chunk)
+    "fwd_chunk_tc": 5 * 256 + 256 + 256,      # Qt, Kt, q, k, v, h -> y
     "fwd_simt": 5 * 256 + 512 + 256,
     "bwd_prep": 2 * 256 + 512 + 3 * 256,      # phi_q, phi_k, log_gamma -> Qt, Kt, e^b
     "bwd_scan_tc": 4 * 256 + 2 * 256,         # Qt, Kt, v, dy -> h, Gt (2 x 32 KB / 128 tokens)
@@ -56,8 +58,6 @@ ALGO_BYTES_PER_TOKEN_HEAD = {
 # source changed since then reports "traffic": null.
 PROFILED_TRAFFIC = {
     # profiles/ncu_step_kernels_llama3_8b.md
-    "fwd_tc": {"bytes_per_token_head": 1981, "source": "hybrid_gated_linear_gb300/csrc/k_fwd_tc.cu",
-               "sha256": "9e04ddd3da7ad346c79e63e8d7f9afdfc485d93d69748f68e7a4fcdd0afdb561"},
     "bwd_prep": {"bytes_per_token_head": 1506, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
                  "sha256": "f45c7cbee44dc30cee745e5d71dd6f87390fddc0727852b9a378a7caa2e47fcf"},
     "bwd_scan_tc": {"bytes_per_token_head": 1277, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",

@@ -7,13 +7,11 @@
 // Gamma its last value, Qt = phi_q e^b, Kt = phi_k e^-b, h_c the state at the start of
 // chunk c and G_c the adjoint of the state at its end.
 //
-//   1. prep   (CUDA cores)  Qt, Kt and e^b in bf16, Gamma in fp32.
-//   2. scan   (tcgen05)     h_{c+1} = diag(e^Gamma_c) (h_c + Kt_c^T V_c),  h_0 = h0
-//                           G_{c-1} = diag(e^Gamma_c) G_c + Qt_c^T dY_c,   G_{nc-1} = 0
-//                           stored as bf16 h_c and Gt_c = diag(e^Gamma_c) G_c.  One CTA per
-//                           (b, h, 32 dv columns, direction): the 128 x 32 chunk products
-//                           come from the tensor cores, the scans run in fp32 registers.
-//                           G_{-1} is the adjoint of h0.
+//   1. prep   (k_gla_states_tc.cu)  Qt, Kt and e^b in bf16, Gamma in fp32.
+//   2. scan   (k_gla_states_tc.cu)  h_{c+1} = diag(e^Gamma_c) (h_c + Kt_c^T V_c), h_0 = h0
+//                                   G_{c-1} = diag(e^Gamma_c) G_c + Qt_c^T dY_c, G_{nc-1} = 0
+//                                   stored as bf16 h_c and Gt_c = diag(e^Gamma_c) G_c;
+//                                   G_{-1} is the adjoint of h0.
 //   3. chunk  (tcgen05)     per (b, h, chunk), every product M = N = K = 128:
 //                             A = dY V^T,  P = Qt Kt^T        (masked to s <= t, bf16)
 //                             dQt = dY h^T + A Kt,   dKt = V Gt^T + A^T Qt
@@ -27,20 +25,15 @@
 // word, drains its copies and MMAs, frees its tensor memory and returns.
 #include "lizard_dev.cuh"
 #include "lizard_internal.h"
-#include "tc_sm100.cuh"
+#include "tc_pipe.cuh"
 
 namespace lz {
 namespace {
 
 using namespace tc;
 
-constexpr int kC = 128;   // chunk
-constexpr int kD = 128;   // dk = dv
-constexpr int kSl = 32;   // dv columns per scan CTA
-constexpr int kSlices = kD / kSl;
-constexpr uint64_t kWaitNs = 1000000000ull;      // 1 s for the exit drains
-constexpr long long kWaitCycles = 2000000000ll;  // ~1 s of SM clock per wait
-constexpr float kMaxLogSum = 80.f;  // |chunk-local log-gate sum| beyond which e^{+-b} overflows
+constexpr int kC = kGlaChunk;  // chunk
+constexpr int kD = 128;        // dk = dv
 
 struct GlaWs {
   bf16 *qt, *kt, *eb;  // [BH][L][128]
@@ -72,54 +65,6 @@ size_t gla_ws_layout(int BH, int L, unsigned char* p, GlaWs* w) {
   return off;
 }
 
-template <int NB>
-struct CtlT {
-  uint64_t bar[NB];
-  uint32_t tmem;
-  int abort;
-};
-
-// Bounded wait: gives up (and raises the CTA's abort flag) after kWaitCycles SM clock
-// cycles, or as soon as another role aborted.
-template <int NB>
-__device__ __forceinline__ bool wait_bar(CtlT<NB>* ctl, int i, uint32_t parity) {
-  uint64_t* b = &ctl->bar[i];
-  if (mbar_try_wait(b, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-#pragma unroll 1
-    for (int k = 0; k < 32; ++k)
-      if (mbar_try_wait(b, parity)) return true;
-    if (*(volatile int*)&ctl->abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
-      *(volatile int*)&ctl->abort = 1;
-      return false;
-    }
-  }
-}
-
-// Waits, with a time limit of its own, for the last armed phase of a barrier; used only
-// while leaving.
-template <int NB>
-__device__ __forceinline__ void drain_bar(CtlT<NB>* ctl, int i, uint32_t armed, uint64_t t0) {
-  if (armed == 0) return;
-  while (!mbar_try_wait(&ctl->bar[i], (armed - 1) & 1))
-    if (globaltimer_ns() - t0 > kWaitNs) break;
-}
-
-// K-major SW128 operand descriptor for k-step j (16 elements) of a 128-row tile stored as
-// two 64-column blocks.
-__device__ __forceinline__ uint64_t desc_k(uint32_t base, int j) {
-  return smem_desc(base + (uint32_t)((j * 16) >> 6) * (kC * 128u) + (uint32_t)((j * 16) & 63) * 2u,
-                   16, 1024, kSw128);
-}
-
-// MN-major SW128 operand descriptor for k-step j of the same tile read transposed: the
-// tile's rows are the K index, its 128 columns the M (or N) index.
-__device__ __forceinline__ uint64_t desc_mn(uint32_t base, int j) {
-  return smem_desc(base + (uint32_t)j * 2048u, kC * 128u, 1024, kSw128);
-}
-
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -137,217 +82,6 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
     }
   }
   return v[0];
-}
-
-// ------------------------------------------------------------------------------------
-// 1. prep: one CTA per (chunk, b*h), thread = key dimension.
-// ------------------------------------------------------------------------------------
-struct PrepP {
-  int L, nc;
-  const bf16 *pq, *pk;
-  const float* lg;
-  GlaWs w;
-  unsigned* status;
-};
-
-__global__ void __launch_bounds__(kD) prep_kernel(const PrepP p) {
-  const int c = blockIdx.x, bh = blockIdx.y, i = threadIdx.x;
-  const int L = p.L, t0 = c * kC, n = min(kC, L - t0);
-  const size_t base = ((size_t)bh * L + t0) * kD + i;
-  const bf16* pq = p.pq + base;
-  const bf16* pk = p.pk + base;
-  const float* lg = p.lg + base;
-  bf16* qt = p.w.qt + base;
-  bf16* kt = p.w.kt + base;
-  bf16* eb = p.w.eb + base;
-  float run = 0.f, big = 0.f;
-  for (int t8 = 0; t8 < n; t8 += 8) {
-    float lv[8], qv[8], kv[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const bool ok = t8 + u < n;
-      const size_t o = (size_t)(t8 + u) * kD;
-      lv[u] = ok ? lg[o] : 0.f;
-      qv[u] = ok ? __bfloat162float(pq[o]) : 0.f;
-      kv[u] = ok ? __bfloat162float(pk[o]) : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (t8 + u < n) {
-        run += lv[u];
-        big = fmaxf(big, fabsf(run));
-        const float e = __expf(run);
-        const size_t o = (size_t)(t8 + u) * kD;
-        qt[o] = __float2bfloat16_rn(qv[u] * e);
-        kt[o] = __float2bfloat16_rn(kv[u] * __expf(-run));
-        eb[o] = __float2bfloat16_rn(e);
-      }
-    }
-  }
-  p.w.gam[((size_t)bh * p.nc + c) * kD + i] = run;
-  // e^{+-b} must stay inside the fp32/bf16 range for the factorised form.
-  if (big > kMaxLogSum) raise_status(p.status, kDevCheck);
-}
-
-// ------------------------------------------------------------------------------------
-// 2. scan: one CTA per (b*h, 32-column slice, direction); warp 0 TMA, warp 1 MMA,
-//    warps 2-5 scan (thread = state row).
-// ------------------------------------------------------------------------------------
-struct ScanMaps {
-  CUtensorMap x0, y0, x1, y1;  // direction 0: Kt, V ; direction 1: Qt, dY
-};
-
-struct ScanP {
-  int L, nc;
-  const float* h0;
-  float* dh0;
-  GlaWs w;
-  unsigned* status;
-};
-
-enum { S_FULL = 0, S_EMPTY = 2, S_DFULL = 4, S_DFREE = 6, S_DONE = 8, S_COUNT };
-constexpr uint32_t kScanX = kC * kD * 2;             // 32 KB: Kt or Qt tile
-constexpr uint32_t kScanY = kC * kSl * 2;            // 8 KB: V or dY slice
-constexpr uint32_t kScanStage = kScanX + kScanY;     // multiple of 1024
-constexpr uint32_t kScanBars = 2 * kScanStage;
-constexpr size_t kScanSmem = kScanBars + 1024 + 1024;
-constexpr int kScanThreads = 6 * 32;
-
-__global__ void __launch_bounds__(kScanThreads, 1)
-scan_kernel(const __grid_constant__ ScanMaps maps, const ScanP p) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  using Ctl = CtlT<S_COUNT>;
-  Ctl* ctl = reinterpret_cast<Ctl*>(sm + kScanBars);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int dir = blockIdx.x & 1;
-  const int sl = (blockIdx.x >> 1) % kSlices;
-  const int bh = blockIdx.x / (2 * kSlices);
-  const int nc = p.nc;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < S_COUNT; ++i)
-      mbar_init(&ctl->bar[i], (i == S_DFREE || i == S_DFREE + 1) ? 128u : 1u);
-    ctl->abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(&ctl->tmem, 64);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = ctl->tmem;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      const CUtensorMap* mx = dir ? &maps.x1 : &maps.x0;
-      const CUtensorMap* my = dir ? &maps.y1 : &maps.y0;
-      uint32_t armed0 = 0, armed1 = 0;
-      bool ok = true;
-      for (int u = 0; u < nc && ok; ++u) {
-        const int c = dir ? nc - 1 - u : u, s = u & 1;
-        if (u >= 2 && !(ok = wait_bar(ctl, S_EMPTY + s, ((u >> 1) - 1) & 1))) break;
-        unsigned char* st = sm + s * kScanStage;
-        mbar_arrive_expect_tx(&ctl->bar[S_FULL + s], kScanStage);
-        tma_load_3d(st, mx, 0, c * kC, bh, &ctl->bar[S_FULL + s]);
-        tma_load_3d(st + kScanX / 2, mx, 64, c * kC, bh, &ctl->bar[S_FULL + s]);
-        tma_load_3d(st + kScanX, my, sl * kSl, c * kC, bh, &ctl->bar[S_FULL + s]);
-        if (s) ++armed1;
-        else ++armed0;
-      }
-      if (!ok) ctl->abort = 1;
-      const uint64_t t0 = globaltimer_ns();
-      drain_bar(ctl, S_FULL, armed0, t0);
-      drain_bar(ctl, S_FULL + 1, armed1, t0);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // D[i][j] = sum_s X[s][i] Y[s][j]: A = X^T (MN-major), B = Y slice (MN-major, 64 B rows)
-      const uint32_t id = idesc_bf16(kD, kSl, true, true);
-      const uint32_t sbase = smem_u32(sm);
-      bool ok = true;
-      for (int u = 0; u < nc && ok; ++u) {
-        const int s = u & 1;
-        if (!(ok = wait_bar(ctl, S_FULL + s, (u >> 1) & 1))) break;
-        if (u >= 2 && !(ok = wait_bar(ctl, S_DFREE + s, ((u >> 1) - 1) & 1))) break;
-        tc_fence_after();
-        const uint32_t xb = sbase + s * kScanStage, yb = xb + kScanX;
-        for (int j = 0; j < kC / 16; ++j)
-          mma_bf16(tmem + s * kSl, desc_mn(xb, j), smem_desc(yb + j * 1024, kC * 64, 512, kSw64),
-                   id, j > 0);
-        mma_commit(&ctl->bar[S_EMPTY + s]);
-        mma_commit(&ctl->bar[S_DFULL + s]);
-      }
-      if (!ok) ctl->abort = 1;
-      mma_commit(&ctl->bar[S_DONE]);
-      drain_bar(ctl, S_DONE, 1, globaltimer_ns());
-    }
-  } else {
-    const int qw = warp & 3;
-    const int i = qw * 32 + lane;  // state row = TMEM lane
-    const uint32_t tl = tmem + ((uint32_t)(qw * 32) << 16);
-    float x[kSl];
-    if (dir == 0 && p.h0) {
-      const float4* src = reinterpret_cast<const float4*>(p.h0 + ((size_t)bh * kD + i) * kD + sl * kSl);
-#pragma unroll
-      for (int k = 0; k < kSl / 4; ++k) {
-        const float4 v = src[k];
-        x[4 * k] = v.x;
-        x[4 * k + 1] = v.y;
-        x[4 * k + 2] = v.z;
-        x[4 * k + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < kSl; ++k) x[k] = 0.f;
-    }
-    bf16* outb = dir ? p.w.gs : p.w.hs;
-    bool ok = true;
-    for (int u = 0; u < nc && ok; ++u) {
-      const int c = dir ? nc - 1 - u : u, s = u & 1;
-      const float g = expf(p.w.gam[((size_t)bh * nc + c) * kD + i]);
-      if (!(ok = wait_bar(ctl, S_DFULL + s, (u >> 1) & 1))) break;
-      tc_fence_after();
-      uint32_t d[kSl];
-      tmem_ld32(tl + s * kSl, d);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&ctl->bar[S_DFREE + s]);
-      if (dir) {
-#pragma unroll
-        for (int k = 0; k < kSl; ++k) x[k] *= g;
-      }
-      uint4* dst = reinterpret_cast<uint4*>(outb + (((size_t)bh * nc + c) * kD + i) * kD + sl * kSl);
-#pragma unroll
-      for (int k = 0; k < kSl / 8; ++k)
-        dst[k] = make_uint4(pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
-                            pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
-      if (dir) {
-#pragma unroll
-        for (int k = 0; k < kSl; ++k) x[k] += __uint_as_float(d[k]);
-      } else {
-#pragma unroll
-        for (int k = 0; k < kSl; ++k) x[k] = g * (x[k] + __uint_as_float(d[k]));
-      }
-    }
-    if (!ok) ctl->abort = 1;
-    if (ok && dir == 1 && p.dh0) {
-      float4* dst = reinterpret_cast<float4*>(p.dh0 + ((size_t)bh * kD + i) * kD + sl * kSl);
-#pragma unroll
-      for (int k = 0; k < kSl / 4; ++k) dst[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 64);
-  }
-  if (threadIdx.x == 0 && ctl->abort) raise_status(p.status, kDevTimeout);
 }
 
 // ------------------------------------------------------------------------------------
@@ -385,7 +119,7 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  using Ctl = CtlT<M_COUNT>;
+  using Ctl = tc::Ctl<M_COUNT>;
   Ctl* ctl = reinterpret_cast<Ctl*>(sm + C_BARS);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nc = p.nc, L = p.L;
@@ -436,13 +170,13 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
       const uint32_t id_nn = idesc_bf16(kC, kD, true, true);
       const uint32_t sb = smem_u32(sm);
       auto mma_kk = [&](uint32_t d, uint32_t a, uint32_t b, bool acc) {
-        for (int j = 0; j < 8; ++j) mma_bf16(tmem + d, desc_k(a, j), desc_k(b, j), id_kk, acc || j > 0);
+        for (int j = 0; j < 8; ++j) mma_bf16(tmem + d, desc_k(a, kC, j), desc_k(b, kC, j), id_kk, acc || j > 0);
       };
       auto mma_kn = [&](uint32_t d, uint32_t a, uint32_t b, bool acc) {
-        for (int j = 0; j < 8; ++j) mma_bf16(tmem + d, desc_k(a, j), desc_mn(b, j), id_kn, acc || j > 0);
+        for (int j = 0; j < 8; ++j) mma_bf16(tmem + d, desc_k(a, kC, j), desc_mn(b, kC, j), id_kn, acc || j > 0);
       };
       auto mma_nn = [&](uint32_t d, uint32_t a, uint32_t b, bool acc) {
-        for (int j = 0; j < 8; ++j) mma_bf16(tmem + d, desc_mn(a, j), desc_mn(b, j), id_nn, acc || j > 0);
+        for (int j = 0; j < 8; ++j) mma_bf16(tmem + d, desc_mn(a, kC, j), desc_mn(b, kC, j), id_nn, acc || j > 0);
       };
       bool ok = wait_bar(ctl, M_LD0, 0);
       if (ok) {
@@ -673,32 +407,20 @@ cudaError_t launch_bwd_gla_tc(const BwdArgs& a, float* dvacc, unsigned char* ws,
   gla_ws_layout(BH, L, ws, &w);
   cudaError_t e;
 
-  PrepP pp{L, nc, static_cast<const bf16*>(a.pq), static_cast<const bf16*>(a.pk), a.lg, w, a.status};
-  trace_begin("bwd_prep", s);
-  prep_kernel<<<dim3(nc, BH), kD, 0, s>>>(pp);
-  trace_end(s);
-  ++*launches;
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  GlaStatesArgs ga{BH, L, a.pq, a.pk, a.lg, a.v, a.dy, a.h0, nullptr, a.dh0,
+                   w.qt, w.kt, w.eb, w.gam, w.hs, w.gs, a.status};
+  if ((e = launch_gla_prep(ga, s, launches)) != cudaSuccess) return e;
+  if ((e = launch_gla_scan(ga, true, s, launches)) != cudaSuccess) return e;
 
   const uint64_t bhl = (uint64_t)BH, Ll = (uint64_t)L, zs = (uint64_t)BH * nc;
-  ScanMaps sm;
-  bool ok = make_tma_map_bf16(&sm.x0, w.kt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_tma_map_bf16(&sm.y0, a.v, kD, Ll, bhl, kSl, kC, CU_TENSOR_MAP_SWIZZLE_64B) &&
-            make_tma_map_bf16(&sm.x1, w.qt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_tma_map_bf16(&sm.y1, a.dy, kD, Ll, bhl, kSl, kC, CU_TENSOR_MAP_SWIZZLE_64B);
   ChunkMaps cm;
-  ok = ok && make_tma_map_bf16(&cm.dy, a.dy, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-       make_tma_map_bf16(&cm.v, a.v, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-       make_tma_map_bf16(&cm.qt, w.qt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-       make_tma_map_bf16(&cm.kt, w.kt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-       make_tma_map_bf16(&cm.hs, w.hs, kD, kD, zs, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-       make_tma_map_bf16(&cm.gs, w.gs, kD, kD, zs, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B);
+  bool ok = make_tma_map_bf16(&cm.dy, a.dy, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&cm.v, a.v, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&cm.qt, w.qt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&cm.kt, w.kt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&cm.hs, w.hs, kD, kD, zs, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&cm.gs, w.gs, kD, kD, zs, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
-
-  ScanP sp{L, nc, a.h0, a.dh0, w, a.status};
-  e = launch_tc(scan_kernel, sm, sp, BH * kSlices * 2, kScanThreads, kScanSmem, "bwd_scan_tc", s);
-  ++*launches;
-  if (e != cudaSuccess) return e;
 
   ChunkP cp{L, nc, w.eb, static_cast<bf16*>(a.dpq), static_cast<bf16*>(a.dpk), a.dlg, dvacc,
             w.rtot, a.status};

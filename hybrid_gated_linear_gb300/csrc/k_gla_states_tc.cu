@@ -1,0 +1,265 @@
+// k_gla_states_tc.cu -- the two passes the chunk-parallel GLA kernels (forward and
+// backward) start from, for bf16 with dk = dv = 128 and 128-token chunks.
+//
+//   prep  (CUDA cores)  b = chunk-local inclusive cumsum of log gamma, Gamma = its last
+//                       value; Qt = phi_q e^b and Kt = phi_k e^-b in bf16 (and e^b when
+//                       asked), Gamma in fp32 ("Lizard", arXiv 2507.09025, Method:
+//                       parallel form with cumulative gate products, absorbed in log space
+//                       into the features).
+//   scan  (tcgen05)     the state at every chunk start (direction 0)
+//                         h_0 = h0,  h_{c+1} = diag(e^Gamma_c) (h_c + Kt_c^T V_c)
+//                       and, for the backward, the adjoint of the state at every chunk
+//                       end (direction 1)
+//                         G_{nc-1} = 0,  G_{c-1} = diag(e^Gamma_c) G_c + Qt_c^T dY_c
+//                       stored as bf16 h_c and Gt_c = diag(e^Gamma_c) G_c; h_nc is h_final
+//                       and G_{-1} the adjoint of h0 (fp32).  One CTA per (b, h, 32 dv
+//                       columns, direction): warp 0 streams the chunks by TMA, warp 1
+//                       issues one M=128 N=32 K=128 MMA per chunk into a double-buffered
+//                       TMEM tile, warps 2-5 (thread = state row) run the scan in fp32
+//                       registers.
+#include "lizard_dev.cuh"
+#include "lizard_internal.h"
+#include "tc_pipe.cuh"
+
+namespace lz {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = kGlaChunk;
+constexpr int kD = 128;
+constexpr int kSl = 32;  // dv columns per scan CTA
+constexpr int kSlices = kD / kSl;
+constexpr float kMaxLogSum = 80.f;  // |chunk-local log-gate sum| beyond which e^{+-b} overflows
+
+// ------------------------------------------------------------------------------------
+// prep: one CTA per (chunk, b*h), thread = key dimension.
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kD) prep_kernel(const GlaStatesArgs p, int nc) {
+  const int c = blockIdx.x, bh = blockIdx.y, i = threadIdx.x;
+  const int L = p.L, t0 = c * kC, n = min(kC, L - t0);
+  const size_t base = ((size_t)bh * L + t0) * kD + i;
+  const bf16* pq = static_cast<const bf16*>(p.pq) + base;
+  const bf16* pk = static_cast<const bf16*>(p.pk) + base;
+  const float* lg = p.lg + base;
+  bf16* qt = p.qt + base;
+  bf16* kt = p.kt + base;
+  bf16* eb = p.eb ? p.eb + base : nullptr;
+  float run = 0.f, big = 0.f;
+  for (int t8 = 0; t8 < n; t8 += 8) {
+    float lv[8], qv[8], kv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool ok = t8 + u < n;
+      const size_t o = (size_t)(t8 + u) * kD;
+      lv[u] = ok ? lg[o] : 0.f;
+      qv[u] = ok ? __bfloat162float(pq[o]) : 0.f;
+      kv[u] = ok ? __bfloat162float(pk[o]) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (t8 + u < n) {
+        run += lv[u];
+        big = fmaxf(big, fabsf(run));
+        const float e = __expf(run);
+        const size_t o = (size_t)(t8 + u) * kD;
+        qt[o] = __float2bfloat16_rn(qv[u] * e);
+        kt[o] = __float2bfloat16_rn(kv[u] * __expf(-run));
+        if (eb) eb[o] = __float2bfloat16_rn(e);
+      }
+    }
+  }
+  p.gam[((size_t)bh * nc + c) * kD + i] = run;
+  // e^{+-b} must stay inside the fp32/bf16 range for the factorised form.
+  if (big > kMaxLogSum) raise_status(p.status, kDevCheck);
+}
+
+// ------------------------------------------------------------------------------------
+// scan
+// ------------------------------------------------------------------------------------
+struct ScanMaps {
+  CUtensorMap x0, y0, x1, y1;  // direction 0: Kt, V ; direction 1: Qt, dY
+};
+
+enum { S_FULL = 0, S_EMPTY = 2, S_DFULL = 4, S_DFREE = 6, S_DONE = 8, S_COUNT };
+constexpr uint32_t kScanX = kC * kD * 2;          // 32 KB: Kt or Qt tile
+constexpr uint32_t kScanY = kC * kSl * 2;         // 8 KB: V or dY slice
+constexpr uint32_t kScanStage = kScanX + kScanY;  // multiple of 1024
+constexpr uint32_t kScanBars = 2 * kScanStage;
+constexpr size_t kScanSmem = kScanBars + 1024 + 1024;
+constexpr int kScanThreads = 6 * 32;
+
+__global__ void __launch_bounds__(kScanThreads, 1)
+scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc, int ndir) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  using C = Ctl<S_COUNT>;
+  C* ctl = reinterpret_cast<C*>(sm + kScanBars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int dir = ndir == 2 ? (blockIdx.x & 1) : 0;
+  const int sl = (blockIdx.x / ndir) % kSlices;
+  const int bh = blockIdx.x / (ndir * kSlices);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S_COUNT; ++i)
+      mbar_init(&ctl->bar[i], (i == S_DFREE || i == S_DFREE + 1) ? 128u : 1u);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem, 64);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const CUtensorMap* mx = dir ? &maps.x1 : &maps.x0;
+      const CUtensorMap* my = dir ? &maps.y1 : &maps.y0;
+      uint32_t armed0 = 0, armed1 = 0;
+      bool ok = true;
+      for (int u = 0; u < nc && ok; ++u) {
+        const int c = dir ? nc - 1 - u : u, s = u & 1;
+        if (u >= 2 && !(ok = wait_bar(ctl, S_EMPTY + s, ((u >> 1) - 1) & 1))) break;
+        unsigned char* st = sm + s * kScanStage;
+        mbar_arrive_expect_tx(&ctl->bar[S_FULL + s], kScanStage);
+        tma_load_3d(st, mx, 0, c * kC, bh, &ctl->bar[S_FULL + s]);
+        tma_load_3d(st + kScanX / 2, mx, 64, c * kC, bh, &ctl->bar[S_FULL + s]);
+        tma_load_3d(st + kScanX, my, sl * kSl, c * kC, bh, &ctl->bar[S_FULL + s]);
+        if (s) ++armed1;
+        else ++armed0;
+      }
+      if (!ok) ctl->abort = 1;
+      const uint64_t t0 = globaltimer_ns();
+      drain_bar(ctl, S_FULL, armed0, t0);
+      drain_bar(ctl, S_FULL + 1, armed1, t0);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // D[i][j] = sum_s X[s][i] Y[s][j]: A = X^T (MN-major), B = Y slice (MN-major, 64 B rows)
+      const uint32_t id = idesc_bf16(kD, kSl, true, true);
+      const uint32_t sbase = smem_u32(sm);
+      bool ok = true;
+      for (int u = 0; u < nc && ok; ++u) {
+        const int s = u & 1;
+        if (!(ok = wait_bar(ctl, S_FULL + s, (u >> 1) & 1))) break;
+        if (u >= 2 && !(ok = wait_bar(ctl, S_DFREE + s, ((u >> 1) - 1) & 1))) break;
+        tc_fence_after();
+        const uint32_t xb = sbase + s * kScanStage, yb = xb + kScanX;
+        for (int j = 0; j < kC / 16; ++j)
+          mma_bf16(tmem + s * kSl, desc_mn(xb, kC, j), smem_desc(yb + j * 1024, kC * 64, 512, kSw64),
+                   id, j > 0);
+        mma_commit(&ctl->bar[S_EMPTY + s]);
+        mma_commit(&ctl->bar[S_DFULL + s]);
+      }
+      if (!ok) ctl->abort = 1;
+      mma_commit(&ctl->bar[S_DONE]);
+      drain_bar(ctl, S_DONE, 1, globaltimer_ns());
+    }
+  } else {
+    const int qw = warp & 3;
+    const int i = qw * 32 + lane;  // state row = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(qw * 32) << 16);
+    float x[kSl];
+    if (dir == 0 && p.h0) {
+      const float4* src = reinterpret_cast<const float4*>(p.h0 + ((size_t)bh * kD + i) * kD + sl * kSl);
+#pragma unroll
+      for (int k = 0; k < kSl / 4; ++k) {
+        const float4 v = src[k];
+        x[4 * k] = v.x;
+        x[4 * k + 1] = v.y;
+        x[4 * k + 2] = v.z;
+        x[4 * k + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < kSl; ++k) x[k] = 0.f;
+    }
+    bf16* outb = dir ? p.gs : p.hs;
+    bool ok = true;
+    for (int u = 0; u < nc && ok; ++u) {
+      const int c = dir ? nc - 1 - u : u, s = u & 1;
+      const float g = expf(p.gam[((size_t)bh * nc + c) * kD + i]);
+      if (!(ok = wait_bar(ctl, S_DFULL + s, (u >> 1) & 1))) break;
+      tc_fence_after();
+      uint32_t d[kSl];
+      tmem_ld32(tl + s * kSl, d);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&ctl->bar[S_DFREE + s]);
+      if (dir) {
+#pragma unroll
+        for (int k = 0; k < kSl; ++k) x[k] *= g;
+      }
+      uint4* dst = reinterpret_cast<uint4*>(outb + (((size_t)bh * nc + c) * kD + i) * kD + sl * kSl);
+#pragma unroll
+      for (int k = 0; k < kSl / 8; ++k)
+        dst[k] = make_uint4(pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
+                            pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
+      if (dir) {
+#pragma unroll
+        for (int k = 0; k < kSl; ++k) x[k] += __uint_as_float(d[k]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < kSl; ++k) x[k] = g * (x[k] + __uint_as_float(d[k]));
+      }
+    }
+    if (!ok) ctl->abort = 1;
+    float* fin = dir ? p.dh0 : p.hf;
+    if (ok && fin) {
+      float4* dst = reinterpret_cast<float4*>(fin + ((size_t)bh * kD + i) * kD + sl * kSl);
+#pragma unroll
+      for (int k = 0; k < kSl / 4; ++k) dst[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+  if (threadIdx.x == 0 && ctl->abort) raise_status(p.status, kDevTimeout);
+}
+
+}  // namespace
+
+cudaError_t launch_gla_prep(const GlaStatesArgs& a, cudaStream_t s, int* launches) {
+  const int nc = (a.L + kC - 1) / kC;
+  trace_begin(a.eb ? "bwd_prep" : "fwd_prep", s);
+  prep_kernel<<<dim3(nc, a.BH), kD, 0, s>>>(a, nc);
+  trace_end(s);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gla_scan(const GlaStatesArgs& a, bool adjoint, cudaStream_t s, int* launches) {
+  const int nc = (a.L + kC - 1) / kC;
+  const uint64_t bhl = (uint64_t)a.BH, Ll = (uint64_t)a.L;
+  ScanMaps m;
+  bool ok = make_tma_map_bf16(&m.x0, a.kt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&m.y0, a.v, kD, Ll, bhl, kSl, kC, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (adjoint) {
+    ok = ok && make_tma_map_bf16(&m.x1, a.qt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_tma_map_bf16(&m.y1, a.dy, kD, Ll, bhl, kSl, kC, CU_TENSOR_MAP_SWIZZLE_64B);
+  } else {
+    m.x1 = m.x0;
+    m.y1 = m.y0;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  const int ndir = adjoint ? 2 : 1;
+  cudaError_t e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kScanSmem);
+  if (e != cudaSuccess) return e;
+  trace_begin(adjoint ? "bwd_scan_tc" : "fwd_scan_tc", s);
+  scan_kernel<<<a.BH * kSlices * ndir, kScanThreads, kScanSmem, s>>>(m, a, nc, ndir);
+  trace_end(s);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+}  // namespace lz

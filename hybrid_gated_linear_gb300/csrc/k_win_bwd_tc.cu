@@ -25,7 +25,7 @@
 // Every wait is bounded as in the other tensor-core kernels.
 #include "lizard_dev.cuh"
 #include "lizard_internal.h"
-#include "tc_sm100.cuh"
+#include "tc_pipe.cuh"
 
 namespace lz {
 namespace {
@@ -36,62 +36,10 @@ constexpr int kB = 128;   // block of queries / keys
 constexpr int kD = 128;   // dk = dv
 constexpr int kBand = 192;
 constexpr int kMetaRows = 16;
-constexpr uint64_t kWaitNs = 1000000000ull;
-constexpr long long kWaitCycles = 2000000000ll;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kThreads = 6 * 32;  // warp 0 TMA, warp 1 MMA, warps 2-5 rows
 
-struct Ctl {
-  uint64_t bar[8];
-  uint32_t tmem;
-  int abort;
-};
-
-__device__ __forceinline__ bool wait_bar(Ctl* ctl, int i, uint32_t parity) {
-  uint64_t* b = &ctl->bar[i];
-  if (mbar_try_wait(b, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-#pragma unroll 1
-    for (int k = 0; k < 32; ++k)
-      if (mbar_try_wait(b, parity)) return true;
-    if (*(volatile int*)&ctl->abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
-      *(volatile int*)&ctl->abort = 1;
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void drain_bar(Ctl* ctl, int i, uint64_t t0) {
-  while (!mbar_try_wait(&ctl->bar[i], 0))
-    if (globaltimer_ns() - t0 > kWaitNs) break;
-}
-
-// K-major SW128 descriptor, k-step j, tile of `rows` rows stored as 64-column blocks.
-__device__ __forceinline__ uint64_t desc_k(uint32_t base, int rows, int j) {
-  return smem_desc(base + (uint32_t)((j * 16) >> 6) * (uint32_t)rows * 128u + (uint32_t)((j * 16) & 63) * 2u,
-                   16, 1024, kSw128);
-}
-
-// MN-major SW128 descriptor, k-step j, tile whose `rows` rows are the K index and whose
-// 128 columns (two 64-column blocks) are the M or N index.
-__device__ __forceinline__ uint64_t desc_mn(uint32_t base, int rows, int j) {
-  return smem_desc(base + (uint32_t)j * 2048u, (uint32_t)rows * 128u, 1024, kSw128);
-}
-
-__device__ __forceinline__ void store16_bf16(unsigned char* tile, int rows, int row, int col, const float (&v)[16]) {
-  uint32_t w[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-  *reinterpret_cast<uint4*>(tile + sw128_offset(row, col, rows)) = make_uint4(w[0], w[1], w[2], w[3]);
-  *reinterpret_cast<uint4*>(tile + sw128_offset(row, col + 8, rows)) = make_uint4(w[4], w[5], w[6], w[7]);
-}
-
-__device__ __forceinline__ void zero16_bf16(unsigned char* tile, int rows, int row, int col) {
-  *reinterpret_cast<uint4*>(tile + sw128_offset(row, col, rows)) = make_uint4(0, 0, 0, 0);
-  *reinterpret_cast<uint4*>(tile + sw128_offset(row, col + 8, rows)) = make_uint4(0, 0, 0, 0);
-}
+using Ctl = tc::Ctl<8>;
 
 struct Params {
   int H, L, M, W, nq;
@@ -167,8 +115,8 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
         tma_load_3d(sm + QS_VM + 2048, &maps.mv, 64, 0, hh, &ctl->bar[Q_LDV]);
       }
       const uint64_t tw = globaltimer_ns();
-      drain_bar(ctl, Q_LDK, tw);
-      drain_bar(ctl, Q_LDV, tw);
+      drain_bar(ctl, Q_LDK, 1, tw);
+      drain_bar(ctl, Q_LDV, 1, tw);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -214,7 +162,7 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
       }
       if (!ok) ctl->abort = 1;
       mma_commit(&ctl->bar[Q_DONE]);
-      drain_bar(ctl, Q_DONE, globaltimer_ns());
+      drain_bar(ctl, Q_DONE, 1, globaltimer_ns());
     }
   } else {
     const int qw = warp & 3;
@@ -414,8 +362,8 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
       tma_load_3d(sm + KS_DYB, &maps.dyb, 0, j0, bh, &ctl->bar[K_LDV]);
       tma_load_3d(sm + KS_DYB + 24576, &maps.dyb, 64, j0, bh, &ctl->bar[K_LDV]);
       const uint64_t tw = globaltimer_ns();
-      drain_bar(ctl, K_LDK, tw);
-      drain_bar(ctl, K_LDV, tw);
+      drain_bar(ctl, K_LDK, 1, tw);
+      drain_bar(ctl, K_LDV, 1, tw);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -444,7 +392,7 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
       }
       if (!ok) ctl->abort = 1;
       mma_commit(&ctl->bar[K_DONE]);
-      drain_bar(ctl, K_DONE, globaltimer_ns());
+      drain_bar(ctl, K_DONE, 1, globaltimer_ns());
     }
   } else {
     const int qw = warp & 3;
@@ -459,7 +407,7 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
       rl[u] = i < L ? p.lse2[(size_t)bh * L + i] : INFINITY;
       rd[u] = i < L ? p.Dw[(size_t)bh * L + i] : 0.f;
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    named_sync(1, 128);
     // query column u <-> query i = j0 + u; this row is seen by u in [jr, jr + W - 1]
     const int g_lo = (32 * qw) >> 4;
     const int g_hi = min(kBand - 1, 32 * qw + 31 + W - 1) >> 4;

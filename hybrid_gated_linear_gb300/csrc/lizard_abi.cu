@@ -72,6 +72,9 @@ const char* lizard_status_string(lizard_status s) {
 
 size_t lizard_fwd_workspace_bytes(const lizard_dims* dims, int32_t W) {
   if (!dims_ok(dims) || W < 1) return 0;
+  const int W_eff = dims->L > 0 && W > dims->L ? dims->L : W;
+  if (lz::fwd_chunk_tc_supported(dims->dk, dims->dv, dims->L, W_eff, dims->M, dims->dtype))
+    return lz::kWsHeader + lz::fwd_chunk_tc_workspace(dims->B * dims->H, dims->L);
   return lz::kWsHeader;
 }
 
@@ -166,10 +169,12 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* phi_q, const 
   const int W_eff = d.L > 0 && W > d.L ? d.L : W;
   lz::FwdArgs a{d.B, d.H, d.L, d.dk, d.dv, d.M, W_eff, resolve_scale(d.scale, d.dk), alpha,
                 phi_q, phi_k, v, log_gamma, q, k, meta_k, meta_v, y, h0, h_final,
-                static_cast<unsigned*>(workspace)};
+                static_cast<unsigned*>(workspace),
+                static_cast<unsigned char*>(workspace) + lz::kWsHeader};
   int launches = 0;
-  e = lz::fwd_tc_supported(a, d.dtype) ? lz::launch_fwd_tc(a, s, &launches)
-                                       : lz::launch_fwd_simt(a, d.dtype, s, &launches);
+  e = lz::fwd_chunk_tc_supported(d.dk, d.dv, d.L, W_eff, d.M, d.dtype)
+          ? lz::launch_fwd_chunk_tc(a, a.ws, s, &launches)
+          : lz::launch_fwd_simt(a, d.dtype, s, &launches);
   g_last_launches = launches;
   return cuda_status(e);
 }

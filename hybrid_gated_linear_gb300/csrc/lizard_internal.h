@@ -10,6 +10,8 @@
 
 namespace lz {
 
+using bf16 = __nv_bfloat16;
+
 // Device status word bits (first word of every workspace).
 enum : unsigned { kDevTimeout = 1u, kDevCheck = 2u };
 
@@ -29,6 +31,7 @@ struct FwdArgs {
   const float* h0;
   float* hf;
   unsigned* status;
+  unsigned char* ws;  // workspace after the header
 };
 
 struct BwdArgs {
@@ -78,9 +81,34 @@ bool make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t dim0, uint64_t
 cudaError_t launch_chunk_cumsum(int units, int L, int dk, int chunk, const float* lg, float* b,
                                 float* gamma_chunk, cudaStream_t s, int* launches);
 cudaError_t launch_fwd_simt(const FwdArgs& a, lizard_dtype dt, cudaStream_t s, int* launches);
-// Tensor-core forward (bf16, dk = dv = 128, W <= 129, M <= 16).
-bool fwd_tc_supported(const FwdArgs& a, lizard_dtype dt);
-cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s, int* launches);
+// Chunk-parallel tensor-core forward (bf16, dk = dv = 128, L > 0, 1 <= W <= 129,
+// M <= 16); scratch of fwd_chunk_tc_workspace(B*H, L) bytes at a.ws.
+bool fwd_chunk_tc_supported(int dk, int dv, int L, int W, int M, lizard_dtype dt);
+size_t fwd_chunk_tc_workspace(int BH, int L);
+cudaError_t launch_fwd_chunk_tc(const FwdArgs& a, unsigned char* ws, cudaStream_t s, int* launches);
+// Chunk length of the chunk-parallel tensor-core GLA kernels.
+constexpr int kGlaChunk = 128;
+
+// Inputs and outputs of the two passes the chunk-parallel GLA kernels start from
+// (k_gla_states_tc.cu); bf16, dk = dv = 128.  qt, kt, eb [BH][L][128] bf16 (eb may be
+// null), gam [BH][nc][128] fp32, hs / gs [BH][nc][128][128] bf16 with nc = ceil(L/128);
+// h0 may be null (zeros); hf (h_final) and dh0 may be null.
+struct GlaStatesArgs {
+  int BH, L;
+  const void *pq, *pk;
+  const float* lg;
+  const void *v, *dy;
+  const float* h0;
+  float *hf, *dh0;
+  bf16 *qt, *kt, *eb;
+  float* gam;
+  bf16 *hs, *gs;
+  unsigned* status;
+};
+cudaError_t launch_gla_prep(const GlaStatesArgs& a, cudaStream_t s, int* launches);
+// Direction 0 (states) always; direction 1 (scaled adjoints) when `adjoint`.
+cudaError_t launch_gla_scan(const GlaStatesArgs& a, bool adjoint, cudaStream_t s, int* launches);
+
 // Tensor-core backward of the GLA branch (bf16, dk = dv = 128, L > 0): writes d_phi_q,
 // d_phi_k, d_log_gamma, d_h0 and the GLA part of dv (fp32 [B*H][L][128]) to dvacc, using
 // bwd_gla_tc_workspace(B*H, L) bytes of scratch at ws (256-byte aligned).
