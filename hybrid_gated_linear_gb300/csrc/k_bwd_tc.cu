@@ -18,8 +18,10 @@
 //                             dV  = Kt Gt + P^T dY
 //                           then d phi_q = dQt e^b, d phi_k = dKt e^-b, and the per-token
 //                           log-gate term r = phi_q d phi_q - phi_k d phi_k = Qt dQt - Kt dKt
-//                           with its sum over the chunk's tokens.
-//   4. suffix (CUDA cores)  d log gamma_t = sum_{t' >= t} r_t'.
+//                           summed from the chunk's end (and its chunk total); outputs are
+//                           staged in shared memory and written by TMA stores.
+//   4. suffix (CUDA cores)  d log gamma_t = sum_{t' >= t} r_t': adds the totals of the later
+//                           chunks.
 //
 // Every wait is bounded; on a timeout the CTA records LIZARD_ERR_TIMEOUT in the status
 // word, drains its copies and MMAs, frees its tensor memory and returns.
@@ -68,42 +70,24 @@ size_t gla_ws_layout(int BH, int L, unsigned char* p, GlaWs* w) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Sums v over the 32 lanes of the warp entry by entry; afterwards lane l holds the total
-// of entry l (reduce-scatter by recursive halving, a fixed order).
-__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int k = 0; k < o; ++k) {
-      const float send = upper ? v[k] : v[k + o];
-      const float keep = upper ? v[k + o] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-    }
-  }
-  return v[0];
-}
-
 // ------------------------------------------------------------------------------------
 // 3. chunk: one CTA per (b*h, chunk); warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 //    (thread = tile row, half of the columns).
 // ------------------------------------------------------------------------------------
 struct ChunkMaps {
-  CUtensorMap dy, v, qt, kt, hs, gs;
+  CUtensorMap dy, v, qt, kt, hs, gs, eb;  // loads
+  CUtensorMap dpq, dpk, dlg, dvo;        // stores
 };
 
 struct ChunkP {
   int L, nc;
-  const bf16* eb;
-  bf16 *dpq, *dpk;
-  float* dlg;
-  float* dvacc;
+  int ahead;  // CTAs per wave: the tile whose inputs this CTA prefetches into L2
   float* rtot;
   unsigned* status;
 };
 
 enum {
-  M_LD0 = 0, M_LD1, M_LD2, M_LD3, M_A, M_P, M_AS, M_PS, M_DQK, M_DV, M_DONE, M_COUNT
+  M_LD0 = 0, M_LD1, M_LD2, M_LD3, M_A, M_P, M_AS, M_PS, M_DQK, M_DV, M_EB, M_DONE, M_COUNT
 };
 constexpr uint32_t kTile = kC * kD * 2;  // 32 KB
 constexpr uint32_t C_DY = 0, C_V = kTile, C_QT = 2 * kTile, C_KT = 3 * kTile, C_HS = 4 * kTile,
@@ -137,7 +121,7 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
 
@@ -160,8 +144,35 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
       tma_load_3d(sm + C_QT + kTile / 2, &maps.qt, 64, t0, bh, &ctl->bar[M_LD3]);
       tma_load_3d(sm + C_KT, &maps.kt, 0, t0, bh, &ctl->bar[M_LD3]);
       tma_load_3d(sm + C_KT + kTile / 2, &maps.kt, 64, t0, bh, &ctl->bar[M_LD3]);
+      // e^b is loaded only once dQt and dKt are done; bring it into L2 now
+      tma_prefetch_l2_3d(&maps.eb, 0, t0, bh);
+      tma_prefetch_l2_3d(&maps.eb, 64, t0, bh);
+      // Once this tile's inputs are in, warm L2 with those of the tile one wave later, so
+      // that its loads overlap this tile's tensor-core and epilogue phases.
+      const int nb = blockIdx.x + p.ahead;
+      if (nb < gridDim.x && wait_bar(ctl, M_LD3, 0)) {
+        const int nbh = nb / nc, nt0 = (nb % nc) * kC, nzs = nb;
+        for (int x = 0; x < kD; x += 64) {
+          tma_prefetch_l2_3d(&maps.dy, x, nt0, nbh);
+          tma_prefetch_l2_3d(&maps.hs, x, 0, nzs);
+          tma_prefetch_l2_3d(&maps.v, x, nt0, nbh);
+          tma_prefetch_l2_3d(&maps.gs, x, 0, nzs);
+          tma_prefetch_l2_3d(&maps.qt, x, nt0, nbh);
+          tma_prefetch_l2_3d(&maps.kt, x, nt0, nbh);
+          tma_prefetch_l2_3d(&maps.eb, x, nt0, nbh);
+        }
+      }
+      // e^b goes over the masked A tile once dQt and dKt are complete
+      uint32_t armed_eb = 0;
+      if (wait_bar(ctl, M_DQK, 0)) {
+        mbar_arrive_expect_tx(&ctl->bar[M_EB], kTile);
+        tma_load_3d(sm + C_HS, &maps.eb, 0, t0, bh, &ctl->bar[M_EB]);
+        tma_load_3d(sm + C_HS + kTile / 2, &maps.eb, 64, t0, bh, &ctl->bar[M_EB]);
+        armed_eb = 1;
+      }
       const uint64_t tw = globaltimer_ns();
       for (int b = M_LD0; b <= M_LD3; ++b) drain_bar(ctl, b, 1, tw);
+      drain_bar(ctl, M_EB, armed_eb, tw);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -220,10 +231,11 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
     const int t = qw * 32 + lane; // tile row
     const bool valid = t < n;
     const uint32_t tl = tmem + ((uint32_t)(qw * 32) << 16);
-    float* red = reinterpret_cast<float*>(sm + C_RED);  // [4][128] column partials of r
+    float* red = reinterpret_cast<float*>(sm + C_RED);  // [8 segments][32] partial sums of r
     bool ok = true;
 
-    // Masked (s <= t) bf16 copy of an M = N = 128 product, K-major rows t.
+    // Masked (s <= t) bf16 copy of this thread's 64 columns of an M = N = 128 product,
+    // K-major rows t.
     auto mask_store = [&](uint32_t tcol, unsigned char* dst) {
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
@@ -260,31 +272,41 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
     fence_proxy_async_smem();
     mbar_arrive(&ctl->bar[M_PS]);
 
-    // d phi_q, d phi_k and the log-gate term
-    if (ok && (ok = wait_bar(ctl, M_DQK, 0))) {
-      tc_fence_after();
-      const size_t row = (size_t)bh * L + t0 + t;
+    // d phi_q, d phi_k, the log-gate term r summed from the chunk's end, and the GLA part
+    // of dv, in four rounds of 32 columns (16 per thread).  Each round is staged in one of
+    // two buffers carved from the operand tiles the MMAs no longer need and written by TMA
+    // stores, which drain while the next round is computed.  e^b arrives by TMA over the
+    // A tile.
+    const bool ready = ok && (ok = wait_bar(ctl, M_DV, 0)) && (ok = wait_bar(ctl, M_EB, 0));
+    if (ready) tc_fence_after();
+    const int et = threadIdx.x - 64;           // 0..255
+    const int scol = et & 31, seg = et >> 5;   // suffix pass: column of the round, 16-row segment
+    const bool issuer = et == 0;
 #pragma unroll 1
-      for (int g = 0; g < 2; ++g) {
-        const int i0 = 64 * hf + 32 * g;
-        uint32_t dq[32], dk[32];
-        tmem_ld32(tl + T_DQ + i0, dq);
-        tmem_ld32(tl + T_DK + i0, dk);
-        uint4 ebv[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-          ebv[m] = valid ? reinterpret_cast<const uint4*>(p.eb + row * kD + i0)[m] : make_uint4(0, 0, 0, 0);
+    for (int R = 0; R < 4; ++R) {
+      // buffer 0: dY tile + first half of V; buffer 1: second half of V + Gt tile
+      unsigned char* sdq = sm + ((R & 1) ? C_V + 16384 : C_DY);
+      unsigned char* sdk = sdq + 8192;
+      unsigned char* srr = sm + ((R & 1) ? C_GS : C_DY + 16384);
+      unsigned char* sdv = srr + 16384;
+      const int cl = 16 * hf;       // columns within the round
+      const int i0 = 32 * R + cl;   // columns of the tile
+      if (ready) {
+        uint32_t dq[16], dk[16];
+        tmem_ld16(tl + T_DQ + i0, dq);
+        tmem_ld16(tl + T_DK + i0, dk);
         tmem_ld_wait();
-        float rr[32];
-        uint4 oq[4], ok4[4];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const uint4 qv = *reinterpret_cast<const uint4*>(sm + C_QT + sw128_offset(t, i0 + 8 * m, kC));
-          const uint4 kv = *reinterpret_cast<const uint4*>(sm + C_KT + sw128_offset(t, i0 + 8 * m, kC));
+        for (int m = 0; m < 2; ++m) {
+          const uint32_t off = sw128_offset(t, i0 + 8 * m, kC);
+          const uint4 qv = *reinterpret_cast<const uint4*>(sm + C_QT + off);
+          const uint4 kv = *reinterpret_cast<const uint4*>(sm + C_KT + off);
+          const uint4 ev = *reinterpret_cast<const uint4*>(sm + C_HS + off);
           const uint32_t qa[4] = {qv.x, qv.y, qv.z, qv.w};
           const uint32_t ka[4] = {kv.x, kv.y, kv.z, kv.w};
-          const uint32_t ea[4] = {ebv[m].x, ebv[m].y, ebv[m].z, ebv[m].w};
+          const uint32_t ea[4] = {ev.x, ev.y, ev.z, ev.w};
           uint32_t wq[4], wk[4];
+          float rr[8];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int k0 = 8 * m + 2 * e;
@@ -293,58 +315,67 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
             const float e0 = bf_lo(ea[e]), e1 = bf_hi(ea[e]);
             wq[e] = pack_bf16x2(q0 * e0, q1 * e1);
             wk[e] = pack_bf16x2(valid ? __fdividef(d0, e0) : 0.f, valid ? __fdividef(d1, e1) : 0.f);
-            rr[k0] = valid ? bf_lo(qa[e]) * q0 - bf_lo(ka[e]) * d0 : 0.f;
-            rr[k0 + 1] = valid ? bf_hi(qa[e]) * q1 - bf_hi(ka[e]) * d1 : 0.f;
+            rr[2 * e] = valid ? bf_lo(qa[e]) * q0 - bf_lo(ka[e]) * d0 : 0.f;
+            rr[2 * e + 1] = valid ? bf_hi(qa[e]) * q1 - bf_hi(ka[e]) * d1 : 0.f;
           }
-          oq[m] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-          ok4[m] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+          *reinterpret_cast<uint4*>(sdq + sw64_offset(t, cl + 8 * m)) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+          *reinterpret_cast<uint4*>(sdk + sw64_offset(t, cl + 8 * m)) = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+          *reinterpret_cast<float4*>(srr + sw128_offset_f32(t, cl + 8 * m, kC)) =
+              make_float4(rr[0], rr[1], rr[2], rr[3]);
+          *reinterpret_cast<float4*>(srr + sw128_offset_f32(t, cl + 8 * m + 4, kC)) =
+              make_float4(rr[4], rr[5], rr[6], rr[7]);
         }
-        if (valid) {
-          uint4* dq_out = reinterpret_cast<uint4*>(p.dpq + row * kD + i0);
-          uint4* dk_out = reinterpret_cast<uint4*>(p.dpk + row * kD + i0);
-          float4* r_out = reinterpret_cast<float4*>(p.dlg + row * kD + i0);
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            dq_out[m] = oq[m];
-            dk_out[m] = ok4[m];
-          }
-#pragma unroll
-          for (int m = 0; m < 8; ++m) r_out[m] = make_float4(rr[4 * m], rr[4 * m + 1], rr[4 * m + 2], rr[4 * m + 3]);
-        }
-        red[qw * kD + i0 + lane] = warp_reduce_scatter32(rr, lane);
-      }
-    }
-    // all 256 epilogue threads meet here exactly once, whatever happened above
-    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-    if (ok && ew < 4) {
-      const int col = ew * 32 + lane;
-      p.rtot[((size_t)bh * nc + c) * kD + col] =
-          red[col] + red[kD + col] + red[2 * kD + col] + red[3 * kD + col];
-    }
-
-    // GLA part of dv
-    if (ok && (ok = wait_bar(ctl, M_DV, 0))) {
-      tc_fence_after();
-#pragma unroll 1
-      for (int g = 0; g < 2; ++g) {
-        const int i0 = 64 * hf + 32 * g;
-        uint32_t r[32];
-        tmem_ld32(tl + T_A + i0, r);
+        uint32_t dv[16];
+        tmem_ld16(tl + T_A + i0, dv);
         tmem_ld_wait();
-        if (valid) {
-          float4* dst = reinterpret_cast<float4*>(p.dvacc + ((size_t)bh * L + t0 + t) * kD + i0);
 #pragma unroll
-          for (int m = 0; m < 8; ++m)
-            dst[m] = make_float4(__uint_as_float(r[4 * m]), __uint_as_float(r[4 * m + 1]),
-                                 __uint_as_float(r[4 * m + 2]), __uint_as_float(r[4 * m + 3]));
-        }
+        for (int m = 0; m < 4; ++m)
+          *reinterpret_cast<float4*>(sdv + sw128_offset_f32(t, cl + 4 * m, kC)) =
+              make_float4(__uint_as_float(dv[4 * m]), __uint_as_float(dv[4 * m + 1]),
+                          __uint_as_float(dv[4 * m + 2]), __uint_as_float(dv[4 * m + 3]));
       }
+      named_sync(1, kEpiThreads);
+      // suffix sums of r down the chunk: 8 segments of 16 rows per column
+      if (ready) {
+        float part = 0.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          part += *reinterpret_cast<const float*>(srr + sw128_offset_f32(16 * seg + u, scol, kC));
+        red[seg * 32 + scol] = part;
+      }
+      named_sync(1, kEpiThreads);
+      if (ready) {
+        float run = 0.f;
+#pragma unroll
+        for (int s2 = 7; s2 > 0; --s2)
+          if (s2 > seg) run += red[s2 * 32 + scol];
+#pragma unroll
+        for (int u = 15; u >= 0; --u) {
+          float* q = reinterpret_cast<float*>(srr + sw128_offset_f32(16 * seg + u, scol, kC));
+          run += *q;
+          *q = run;
+        }
+        if (seg == 0) p.rtot[((size_t)bh * nc + c) * kD + 32 * R + scol] = run;
+      }
+      fence_proxy_async_smem();
+      named_sync(1, kEpiThreads);
+      if (ready && issuer) {
+        // rows at or beyond L are clipped by the stores
+        tma_store_3d(&maps.dpq, sdq, 32 * R, t0, bh);
+        tma_store_3d(&maps.dpk, sdk, 32 * R, t0, bh);
+        tma_store_3d(&maps.dlg, srr, 32 * R, t0, bh);
+        tma_store_3d(&maps.dvo, sdv, 32 * R, t0, bh);
+        bulk_commit();
+        bulk_wait_read_prev();  // the other buffer (round R-1) has been read
+      }
+      named_sync(1, kEpiThreads);
     }
+    if (ready && issuer) bulk_wait_read();
     if (!ok) ctl->abort = 1;
   }
 
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -353,31 +384,18 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
 }
 
 // ------------------------------------------------------------------------------------
-// 4. suffix: one CTA per (chunk, b*h), thread = key dimension; r is replaced in place by
-//    its suffix sum over the sequence.
+// 4. suffix: one CTA per (chunk, b*h), thread = key dimension; adds the sums of the later
+//    chunks to the in-chunk suffix sums.
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kD) suffix_kernel(int L, int nc, float* dlg, const float* rtot) {
   const int c = blockIdx.x, bh = blockIdx.y, i = threadIdx.x;
+  if (c == nc - 1) return;
   float carry = 0.f;
   for (int c2 = nc - 1; c2 > c; --c2) carry += rtot[((size_t)bh * nc + c2) * kD + i];
   const int t0 = c * kC, n = min(kC, L - t0);
   float* r = dlg + ((size_t)bh * L + t0) * kD + i;
-  for (int tb = n; tb > 0; tb -= 8) {
-    float v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int tt = tb - 1 - u;
-      v[u] = tt >= 0 ? r[(size_t)tt * kD] : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int tt = tb - 1 - u;
-      if (tt >= 0) {
-        carry += v[u];
-        r[(size_t)tt * kD] = carry;
-      }
-    }
-  }
+#pragma unroll 8
+  for (int t = 0; t < n; ++t) r[(size_t)t * kD] += carry;
 }
 
 template <typename K, typename M, typename P>
@@ -419,11 +437,15 @@ cudaError_t launch_bwd_gla_tc(const BwdArgs& a, float* dvacc, unsigned char* ws,
             make_tma_map_bf16(&cm.qt, w.qt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
             make_tma_map_bf16(&cm.kt, w.kt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
             make_tma_map_bf16(&cm.hs, w.hs, kD, kD, zs, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_tma_map_bf16(&cm.gs, w.gs, kD, kD, zs, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B);
+            make_tma_map_bf16(&cm.gs, w.gs, kD, kD, zs, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&cm.eb, w.eb, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&cm.dpq, a.dpq, kD, Ll, bhl, 32, kC, CU_TENSOR_MAP_SWIZZLE_64B) &&
+            make_tma_map_bf16(&cm.dpk, a.dpk, kD, Ll, bhl, 32, kC, CU_TENSOR_MAP_SWIZZLE_64B) &&
+            make_tma_map_f32(&cm.dlg, a.dlg, kD, Ll, bhl, 32, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_f32(&cm.dvo, dvacc, kD, Ll, bhl, 32, kC, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
 
-  ChunkP cp{L, nc, w.eb, static_cast<bf16*>(a.dpq), static_cast<bf16*>(a.dpk), a.dlg, dvacc,
-            w.rtot, a.status};
+  ChunkP cp{L, nc, ctas_per_wave(1), w.rtot, a.status};
   e = launch_tc(chunk_kernel, cm, cp, BH * nc, kChunkThreads, kChunkSmem, "bwd_chunk_tc", s);
   ++*launches;
   if (e != cudaSuccess) return e;

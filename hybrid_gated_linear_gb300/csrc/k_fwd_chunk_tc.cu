@@ -94,7 +94,7 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
 
@@ -329,7 +329,7 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
   }
 
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

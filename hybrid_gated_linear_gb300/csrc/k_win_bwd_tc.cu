@@ -89,7 +89,7 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
 
@@ -300,7 +300,7 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
   }
 
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -345,7 +345,7 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
 
@@ -478,7 +478,7 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
   }
 
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

@@ -75,6 +75,12 @@ bool tma_encode_available();
 // outside the tensor read as zeros.
 bool make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t dim0, uint64_t dim1,
                        uint64_t dim2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw);
+// Same for fp32 elements.
+bool make_tma_map_f32(CUtensorMap* m, const void* base, uint64_t dim0, uint64_t dim1,
+                      uint64_t dim2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw);
+
+// Number of SMs of the current device times `per_sm` (cached per device).
+int ctas_per_wave(int per_sm);
 
 // Launchers: return the first CUDA error and add the number of kernels they enqueued
 // to *launches.

@@ -28,19 +28,47 @@ EncodeTiled get_encode() {
 }
 }  // namespace
 
+int ctas_per_wave(int per_sm) {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148 * per_sm;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev] * per_sm;
+}
+
 bool tma_encode_available() { return get_encode() != nullptr; }
 
-bool make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t dim0, uint64_t dim1,
-                       uint64_t dim2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
+namespace {
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void* base,
+              uint64_t dim0, uint64_t dim1, uint64_t dim2, uint32_t box0, uint32_t box1,
+              CUtensorMapSwizzle sw) {
   EncodeTiled enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[3] = {dim0, dim1, dim2};
-  cuuint64_t strides[2] = {dim0 * 2, dim0 * dim1 * 2};
+  cuuint64_t strides[2] = {dim0 * esize, dim0 * dim1 * esize};
   cuuint32_t box[3] = {box0, box1, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool make_tma_map_f32(CUtensorMap* m, const void* base, uint64_t dim0, uint64_t dim1,
+                      uint64_t dim2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dim0, dim1, dim2, box0, box1, sw);
+}
+
+bool make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t dim0, uint64_t dim1,
+                       uint64_t dim2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dim0, dim1, dim2, box0, box1, sw);
 }
 
 }  // namespace lz

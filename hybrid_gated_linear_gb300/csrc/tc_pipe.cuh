@@ -89,12 +89,31 @@ __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
+// Waits until the committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Same, but leaves the most recently committed group pending.
+__device__ __forceinline__ void bulk_wait_read_prev() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// Named barrier over `n` threads (a multiple of 32) of the CTA.
+// CTA barriers.  bar.sync counts whole warps, so a warp that reaches it with some lanes
+// still inside a single-lane role (the TMA producer, the MMA issuer) would let the
+// barrier complete early; every warp reconverges first.
+__device__ __forceinline__ void cta_sync() {
+  __syncwarp();
+  __syncthreads();
+}
+
+// Named barrier over `n` threads (whole warps) of the CTA.
 __device__ __forceinline__ void named_sync(int id, int n) {
+  __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 

@@ -98,6 +98,14 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Prefetch of a tensor tile into L2 (no shared-memory destination, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -245,6 +253,15 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t
   const uint32_t blk = col >> 6, c = col & 63;
   const uint32_t chunk = (c >> 3) ^ (row & 7);
   return blk * rows * 128u + row * 128u + chunk * 16u + (c & 7) * 2u;
+}
+
+// Same for fp32 elements: rows of 128 B hold 32 elements; wider tiles are consecutive
+// 32-column blocks of `rows` rows each.
+__host__ __device__ __forceinline__ uint32_t sw128_offset_f32(uint32_t row, uint32_t col,
+                                                              uint32_t rows) {
+  const uint32_t blk = col >> 5, c = col & 31;
+  const uint32_t chunk = (c >> 2) ^ (row & 7);
+  return blk * rows * 128u + row * 128u + chunk * 16u + (c & 3) * 4u;
 }
 
 // Same for a 64-byte-swizzled tile whose rows hold 32 elements (512-byte atoms of 8 rows).
