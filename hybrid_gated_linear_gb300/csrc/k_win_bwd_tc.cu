@@ -43,6 +43,7 @@ using Ctl = tc::Ctl<8>;
 
 struct Params {
   int H, L, M, W, nq;
+  int ahead;  // CTAs per wave: the tile whose inputs a CTA prefetches into L2
   float scale, alpha;
   float* lse2;      // [BH][L]  log2-domain log-sum-exp of each query row
   float* Dw;        // [BH][L]
@@ -56,7 +57,8 @@ struct Params {
 // query kernel
 // ------------------------------------------------------------------------------------
 struct QMaps {
-  CUtensorMap q, dy, kb, vb, mk, mv;
+  CUtensorMap q, dy, kb, vb, mk, mv;  // loads
+  CUtensorMap dqo;                    // store
 };
 
 enum { Q_LDK = 0, Q_LDV, Q_ZF, Q_DPF, Q_DS, Q_OUT, Q_DONE };
@@ -113,6 +115,17 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
       if (M > 0) {
         tma_load_3d(sm + QS_VM, &maps.mv, 0, 0, hh, &ctl->bar[Q_LDV]);
         tma_load_3d(sm + QS_VM + 2048, &maps.mv, 64, 0, hh, &ctl->bar[Q_LDV]);
+      }
+      // warm L2 with the inputs of the tile one wave later
+      const int nb = blockIdx.x + p.ahead;
+      if (nb < gridDim.x && wait_bar(ctl, Q_LDV, 0)) {
+        const int nbh = nb / p.nq, ni0 = (nb % p.nq) * kB;
+        for (int x = 0; x < kD; x += 64) {
+          tma_prefetch_l2_3d(&maps.q, x, ni0, nbh);
+          tma_prefetch_l2_3d(&maps.kb, x, ni0 - 64, nbh);
+          tma_prefetch_l2_3d(&maps.dy, x, ni0, nbh);
+          tma_prefetch_l2_3d(&maps.vb, x, ni0 - 64, nbh);
+        }
       }
       const uint64_t tw = globaltimer_ns();
       drain_bar(ctl, Q_LDK, 1, tw);
@@ -262,24 +275,21 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
     }
     if (ok && (ok = wait_bar(ctl, Q_OUT, 0))) {
       tc_fence_after();
+      // dq staged over the query tile (free once the meta products are done)
 #pragma unroll 1
       for (int c = 0; c < kD; c += 32) {
         uint32_t v[32];
         tmem_ld32(tl + TQ_DQ + c, v);
         tmem_ld_wait();
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.dq + ((size_t)bh * L + i) * kD + c);
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            uint32_t w[4];
+        for (int h = 0; h < 2; ++h) {
+          float w[16];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf16x2(p.scale * __uint_as_float(v[8 * m + 2 * e]),
-                                 p.scale * __uint_as_float(v[8 * m + 2 * e + 1]));
-            dst[m] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
+          for (int e = 0; e < 16; ++e) w[e] = p.scale * __uint_as_float(v[16 * h + e]);
+          store16_bf16(sm + QS_Q, kB, r, c + 16 * h, w);
         }
       }
+      fence_proxy_async_smem();
       if (M > 0) {
         // lane r of the meta products = feature dimension r
         uint32_t mk[16], mv[16];
@@ -295,6 +305,14 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
           }
         }
       }
+    }
+    named_sync(1, 128);
+    if (ok && threadIdx.x == 64) {
+      // rows at or beyond L are clipped by the store
+      tma_store_3d(&maps.dqo, sm + QS_Q, 0, i0, bh);
+      tma_store_3d(&maps.dqo, sm + QS_Q + 16384, 64, i0, bh);
+      bulk_commit();
+      bulk_wait_read();
     }
     if (!ok) ctl->abort = 1;
   }
@@ -312,10 +330,13 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
 // key kernel
 // ------------------------------------------------------------------------------------
 struct KMaps {
-  CUtensorMap k, v, qb, dyb;
+  CUtensorMap k, v, qb, dyb, dva;  // loads (dva: the GLA part of dv, fp32)
+  CUtensorMap dvo, dko;            // stores
 };
 
-enum { K_LDK = 0, K_LDV, K_SF, K_PDS, K_OUT, K_DONE };
+enum { K_LDK = 0, K_LDV, K_SF, K_PDS, K_OUT, K_DVA, K_DONE };
+// after the MMAs: dv and dk staged over K and V, the GLA part of dv (fp32) over the bands
+constexpr uint32_t KS_DVS = 0, KS_DKS = 32768, KS_DVA = 65536;
 constexpr uint32_t KS_K = 0, KS_V = 32768, KS_PT = 0 /* over K and V */, KS_QB = 65536,
                    KS_DYB = KS_QB + 49152, KS_DST = KS_DYB + 49152, KS_ROW = KS_DST + 49152,
                    KS_BARS = KS_ROW + 2048;
@@ -361,9 +382,30 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
       tma_load_3d(sm + KS_V + 16384, &maps.v, 64, j0, bh, &ctl->bar[K_LDV]);
       tma_load_3d(sm + KS_DYB, &maps.dyb, 0, j0, bh, &ctl->bar[K_LDV]);
       tma_load_3d(sm + KS_DYB + 24576, &maps.dyb, 64, j0, bh, &ctl->bar[K_LDV]);
+      for (int x = 0; x < kD; x += 32) tma_prefetch_l2_3d(&maps.dva, x, j0, bh);
+      // warm L2 with the inputs of the tile one wave later
+      const int nb = blockIdx.x + p.ahead;
+      if (nb < gridDim.x && wait_bar(ctl, K_LDV, 0)) {
+        const int nbh = nb / p.nq, nj0 = (nb % p.nq) * kB;
+        for (int x = 0; x < kD; x += 64) {
+          tma_prefetch_l2_3d(&maps.k, x, nj0, nbh);
+          tma_prefetch_l2_3d(&maps.qb, x, nj0, nbh);
+          tma_prefetch_l2_3d(&maps.v, x, nj0, nbh);
+          tma_prefetch_l2_3d(&maps.dyb, x, nj0, nbh);
+        }
+      }
+      // the GLA part of dv, once the shared memory of the band tiles is free
+      uint32_t armed = 0;
+      if (wait_bar(ctl, K_OUT, 0)) {
+        mbar_arrive_expect_tx(&ctl->bar[K_DVA], kB * kD * 4);
+        for (int x = 0; x < kD; x += 32)
+          tma_load_3d(sm + KS_DVA + x * 512, &maps.dva, x, j0, bh, &ctl->bar[K_DVA]);
+        armed = 1;
+      }
       const uint64_t tw = globaltimer_ns();
       drain_bar(ctl, K_LDK, 1, tw);
       drain_bar(ctl, K_LDV, 1, tw);
+      drain_bar(ctl, K_DVA, armed, tw);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -443,7 +485,8 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
     tc_fence_before();
     fence_proxy_async_smem();
     mbar_arrive(&ctl->bar[K_PDS]);
-    if (ok && (ok = wait_bar(ctl, K_OUT, 0))) {
+    const bool ready = ok && (ok = wait_bar(ctl, K_OUT, 0)) && (ok = wait_bar(ctl, K_DVA, 0));
+    if (ready) {
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < kD; c += 32) {
@@ -451,28 +494,36 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
         tmem_ld32(tl + TK_DV + c, v);
         tmem_ld32(tl + TK_DK + c, k);
         tmem_ld_wait();
-        if (valid) {
-          const size_t row = ((size_t)bh * L + j) * kD + c;
-          const float4* ga = reinterpret_cast<const float4*>(p.dvacc + row);
-          uint4* dvo = reinterpret_cast<uint4*>(p.dv + row);
-          uint4* dko = reinterpret_cast<uint4*>(p.dk + row);
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const float4 a0 = ga[2 * m], a1 = ga[2 * m + 1];
-            const float gv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            uint32_t wv[4], wk[4];
+        for (int h = 0; h < 2; ++h) {
+          float wv[16], wk[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 g = *reinterpret_cast<const float4*>(
+                sm + KS_DVA + sw128_offset_f32(jr, c + 16 * h + 4 * q, kB));
+            const float ga[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              wv[e] = pack_bf16x2(fmaf(p.alpha, __uint_as_float(v[8 * m + 2 * e]), gv[2 * e]),
-                                  fmaf(p.alpha, __uint_as_float(v[8 * m + 2 * e + 1]), gv[2 * e + 1]));
-              wk[e] = pack_bf16x2(p.scale * __uint_as_float(k[8 * m + 2 * e]),
-                                  p.scale * __uint_as_float(k[8 * m + 2 * e + 1]));
+              const int k0 = 16 * h + 4 * q + e;
+              wv[4 * q + e] = fmaf(p.alpha, __uint_as_float(v[k0]), ga[e]);
+              wk[4 * q + e] = p.scale * __uint_as_float(k[k0]);
             }
-            dvo[m] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-            dko[m] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
           }
+          store16_bf16(sm + KS_DVS, kB, jr, c + 16 * h, wv);
+          store16_bf16(sm + KS_DKS, kB, jr, c + 16 * h, wk);
         }
       }
+      fence_proxy_async_smem();
+    }
+    named_sync(1, 128);
+    if (ready && threadIdx.x == 64) {
+      // rows at or beyond L are clipped by the stores
+      tma_store_3d(&maps.dvo, sm + KS_DVS, 0, j0, bh);
+      tma_store_3d(&maps.dvo, sm + KS_DVS + 16384, 64, j0, bh);
+      tma_store_3d(&maps.dko, sm + KS_DKS, 0, j0, bh);
+      tma_store_3d(&maps.dko, sm + KS_DKS + 16384, 64, j0, bh);
+      bulk_commit();
+      bulk_wait_read();
     }
     if (!ok) ctl->abort = 1;
   }
@@ -538,7 +589,11 @@ cudaError_t launch_bwd_win_tc(const BwdArgs& a, const float* dvacc, float* lse2,
             make_tma_map_bf16(&km.k, a.k, kD, Ll, bhl, 64, kB, CU_TENSOR_MAP_SWIZZLE_128B) &&
             make_tma_map_bf16(&km.v, a.v, kD, Ll, bhl, 64, kB, CU_TENSOR_MAP_SWIZZLE_128B) &&
             make_tma_map_bf16(&km.qb, a.q, kD, Ll, bhl, 64, kBand, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_tma_map_bf16(&km.dyb, a.dy, kD, Ll, bhl, 64, kBand, CU_TENSOR_MAP_SWIZZLE_128B);
+            make_tma_map_bf16(&km.dyb, a.dy, kD, Ll, bhl, 64, kBand, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_f32(&km.dva, dvacc, kD, Ll, bhl, 32, kB, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&km.dvo, a.dvv, kD, Ll, bhl, 64, kB, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&km.dko, a.dk_, kD, Ll, bhl, 64, kB, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tma_map_bf16(&qm.dqo, a.dq, kD, Ll, bhl, 64, kB, CU_TENSOR_MAP_SWIZZLE_128B);
   if (a.M > 0) {
     ok = ok && make_tma_map_bf16(&qm.mk, a.mk, kD, a.M, a.H, 64, kMetaRows, CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_tma_map_bf16(&qm.mv, a.mv, kD, a.M, a.H, 64, kMetaRows, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -553,6 +608,7 @@ cudaError_t launch_bwd_win_tc(const BwdArgs& a, const float* dvacc, float* lse2,
   p.M = a.M;
   p.W = a.W;
   p.nq = nq;
+  p.ahead = ctas_per_wave(1);
   p.scale = a.scale;
   p.alpha = a.alpha;
   p.lse2 = lse2;
