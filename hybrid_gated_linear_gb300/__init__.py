@@ -23,6 +23,7 @@ __all__ = [
     "lizard_workspace_init", "lizard_check_device_errors", "lizard_status_string",
     "lizard_abi_version", "lizard_last_launch_count", "lizard_trace_enable", "lizard_trace_read",
     "lizard_decode_step_noalloc", "LIZARD_NOALLOC_MAX_SEQUENCES",
+    "lizard_attn_fwd_bwd_host", "lizard_fwd_bwd_host_workspace_bytes",
     "LIZARD_F32", "LIZARD_BF16", "EXPORTED_SYMBOLS",
 ]
 
@@ -35,7 +36,7 @@ EXPORTED_SYMBOLS = (
     "lizard_fwd_workspace_bytes", "lizard_bwd_workspace_bytes", "lizard_decode_workspace_bytes",
     "lizard_workspace_init", "lizard_check_device_errors", "lizard_status_string",
     "lizard_abi_version", "lizard_last_launch_count", "lizard_trace_enable", "lizard_trace_read",
-    "lizard_decode_step_noalloc",
+    "lizard_decode_step_noalloc", "lizard_attn_fwd_bwd_host", "lizard_fwd_bwd_host_workspace_bytes",
 )
 
 STATUS_NAMES = {0: "LIZARD_OK", 1: "LIZARD_ERR_INVALID_ARG", 2: "LIZARD_ERR_UNSUPPORTED",
@@ -98,6 +99,8 @@ def library():
                 "lizard_trace_enable": (I32, [I32]),
                 "lizard_trace_read": (I32, [ctypes.c_char_p, I32, ctypes.POINTER(F), I32]),
                 "lizard_decode_step_noalloc": (I32, [DDP] + [P] * 8 + [I32, F] + [P] * 5 + [P]),
+                "lizard_fwd_bwd_host_workspace_bytes": (SZ, [DP, I32]),
+                "lizard_attn_fwd_bwd_host": (I32, [DP] + [P] * 8 + [I32, F] + [P] * 13 + [P, SZ, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -165,6 +168,10 @@ def lizard_fwd_workspace_bytes(dims: lizard_dims, W: int) -> int:
 
 def lizard_bwd_workspace_bytes(dims: lizard_dims, W: int) -> int:
     return library().lizard_bwd_workspace_bytes(ctypes.byref(dims), W)
+
+
+def lizard_fwd_bwd_host_workspace_bytes(dims: lizard_dims, W: int) -> int:
+    return library().lizard_fwd_bwd_host_workspace_bytes(ctypes.byref(dims), W)
 
 
 def lizard_decode_workspace_bytes(dims: lizard_decode_dims) -> int:
@@ -255,3 +262,19 @@ def lizard_decode_step_noalloc(dims: lizard_decode_dims, phi_q, phi_k, v, log_ga
                                               _ptr(h), _ptr(k_ring), _ptr(v_ring), _ptr(pos),
                                               _ptr(y), _stream(stream))
     _check(st, "lizard_decode_step_noalloc")
+
+
+def lizard_attn_fwd_bwd_host(dims: lizard_dims, phi_q, phi_k, v, log_gamma, q, k, meta_k, meta_v,
+                             W: int, alpha: float, h0, dy, y, h_final, d_phi_q, d_phi_k, d_v,
+                             d_log_gamma, d_q, d_k, d_meta_k, d_meta_v, d_h0, workspace,
+                             stream=None):
+    """Forward + backward with every tensor in host memory (CPU tensors, pinned for overlap);
+    ``workspace`` is a device tensor of lizard_fwd_bwd_host_workspace_bytes bytes.  Returns
+    once the work is queued; synchronise the stream before reading the outputs."""
+    st = library().lizard_attn_fwd_bwd_host(
+        ctypes.byref(dims), _ptr(phi_q), _ptr(phi_k), _ptr(v), _ptr(log_gamma), _ptr(q), _ptr(k),
+        _ptr(meta_k), _ptr(meta_v), int(W), float(alpha), _ptr(h0), _ptr(dy), _ptr(y),
+        _ptr(h_final), _ptr(d_phi_q), _ptr(d_phi_k), _ptr(d_v), _ptr(d_log_gamma), _ptr(d_q),
+        _ptr(d_k), _ptr(d_meta_k), _ptr(d_meta_v), _ptr(d_h0), _ptr(workspace),
+        _ws_bytes(workspace), _stream(stream))
+    _check(st, "lizard_attn_fwd_bwd_host")

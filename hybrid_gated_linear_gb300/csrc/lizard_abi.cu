@@ -5,6 +5,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "lizard_internal.h"
 
 namespace {
@@ -48,6 +50,90 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 lizard_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LIZARD_OK : LIZARD_ERR_CUDA; }
+
+cudaError_t dispatch_fwd(const lz::FwdArgs& a, lizard_dtype dt, cudaStream_t s, int* launches) {
+  return lz::fwd_chunk_tc_supported(a.dk, a.dv, a.L, a.W, a.M, dt)
+             ? lz::launch_fwd_chunk_tc(a, a.ws, s, launches)
+             : lz::launch_fwd_simt(a, dt, s, launches);
+}
+
+// ---------------------------------------------------------------------------------------
+// Host-memory forward + backward: head slices pipelined over three streams.
+// ---------------------------------------------------------------------------------------
+int host_slice_heads(int H) { return (H + 7) / 8; }  // at most 8 slices
+
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
+  bool ready = false;
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[64];
+
+// The copy streams and events of the current device, created on first use and kept for
+// the life of the process.  Called with g_pipe_mu held.
+HostPipe* host_pipe() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  HostPipe& p = g_pipe[dev];
+  if (!p.ready) {
+    bool ok = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming) == cudaSuccess;
+    for (int b = 0; b < 2 && ok; ++b)
+      ok = cudaEventCreateWithFlags(&p.ev_in[b], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&p.ev_comp[b], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&p.ev_out[b], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) return nullptr;
+    p.ready = true;
+  }
+  return &p;
+}
+
+// Byte offsets of one slice buffer (device) for Hs heads.
+struct SliceLayout {
+  enum { PQ, PK, V, Q, K, DY, LG, H0, MK, MV, Y, DPQ, DPK, DV, DQ, DK, DLG, HF, DH0, DMK, DMV, N };
+  size_t off[N];
+  size_t bytes;
+};
+
+SliceLayout slice_layout(const lizard_dims& d, int Hs, bool h0, bool hf, bool dh0) {
+  const size_t es = elem_size(d.dtype);
+  const size_t tokT = (size_t)d.B * Hs * d.L * d.dk * es, tokF = (size_t)d.B * Hs * d.L * d.dk * 4;
+  const size_t st = (size_t)d.B * Hs * d.dk * d.dv * 4;
+  const size_t meT = (size_t)Hs * d.M * d.dk * es, meF = (size_t)Hs * d.M * d.dk * 4;
+  const size_t sz[SliceLayout::N] = {tokT, tokT, tokT, tokT, tokT, tokT, tokF, h0 ? st : 0, meT, meT,
+                                     tokT, tokT, tokT, tokT, tokT, tokT, tokF, hf ? st : 0,
+                                     dh0 ? st : 0, meF, meF};
+  SliceLayout l;
+  size_t o = 0;
+  for (int i = 0; i < SliceLayout::N; ++i) {
+    l.off[i] = o;
+    o += lz::align_up(sz[i], 256);
+  }
+  l.bytes = o;
+  return l;
+}
+
+size_t host_op_scratch(const lizard_dims& d, int W, int Hs) {
+  lizard_dims ds = d;
+  ds.H = Hs;
+  const size_t f = lizard_fwd_workspace_bytes(&ds, W), b = lizard_bwd_workspace_bytes(&ds, W);
+  const size_t m = f > b ? f : b;
+  return m > lz::kWsHeader ? m - lz::kWsHeader : 0;
+}
+
+// Copies heads [h0, h0+hs) of a [B, H, rows] tensor (rows bytes per head) between host and
+// a [B, hs, rows] device buffer.
+cudaError_t copy_heads(void* dst, const void* src, const lizard_dims& d, int h0, int hs,
+                       size_t row, bool to_device, cudaStream_t s) {
+  if (!dst || !src || row == 0) return cudaSuccess;
+  if (to_device)
+    return cudaMemcpy2DAsync(dst, hs * row, static_cast<const char*>(src) + h0 * row, d.H * row,
+                             hs * row, d.B, cudaMemcpyHostToDevice, s);
+  return cudaMemcpy2DAsync(static_cast<char*>(dst) + h0 * row, d.H * row, src, hs * row, hs * row,
+                           d.B, cudaMemcpyDeviceToHost, s);
+}
 
 }  // namespace
 
@@ -172,9 +258,7 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* phi_q, const 
                 static_cast<unsigned*>(workspace),
                 static_cast<unsigned char*>(workspace) + lz::kWsHeader};
   int launches = 0;
-  e = lz::fwd_chunk_tc_supported(d.dk, d.dv, d.L, W_eff, d.M, d.dtype)
-          ? lz::launch_fwd_chunk_tc(a, a.ws, s, &launches)
-          : lz::launch_fwd_simt(a, d.dtype, s, &launches);
+  e = dispatch_fwd(a, d.dtype, s, &launches);
   g_last_launches = launches;
   return cuda_status(e);
 }
@@ -283,6 +367,143 @@ lizard_status lizard_decode_step(const lizard_decode_dims* dims, const void* phi
                 static_cast<unsigned*>(workspace)};
   int launches = 0;
   cudaError_t e = lz::launch_decode(a, d.dtype, (cudaStream_t)stream, &launches);
+  g_last_launches = launches;
+  return cuda_status(e);
+}
+
+size_t lizard_fwd_bwd_host_workspace_bytes(const lizard_dims* dims, int32_t W) {
+  if (!dims_ok(dims) || W < 1 || shape_supported(dims->dk, dims->dv) != LIZARD_OK) return 0;
+  const int Hs = host_slice_heads(dims->H);
+  const SliceLayout l = slice_layout(*dims, Hs, true, true, true);
+  return lz::kWsHeader + lz::align_up(host_op_scratch(*dims, W, Hs), 256) + 2 * l.bytes;
+}
+
+lizard_status lizard_attn_fwd_bwd_host(const lizard_dims* dims, const void* phi_q,
+                                       const void* phi_k, const void* v, const float* log_gamma,
+                                       const void* q, const void* k, const void* meta_k,
+                                       const void* meta_v, int32_t W, float alpha,
+                                       const float* h0, const void* dy, void* y, float* h_final,
+                                       void* d_phi_q, void* d_phi_k, void* d_v,
+                                       float* d_log_gamma, void* d_q, void* d_k, float* d_meta_k,
+                                       float* d_meta_v, float* d_h0, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  g_last_launches = 0;
+  if (!dims_ok(dims) || W < 1 || !isfinite(alpha)) return LIZARD_ERR_INVALID_ARG;
+  const lizard_dims& d = *dims;
+  const bool tok = d.L > 0;
+  const void* tok_ptrs[] = {phi_q, phi_k, v, log_gamma, q, k, dy, y,
+                            d_phi_q, d_phi_k, d_v, d_log_gamma, d_q, d_k};
+  for (const void* p : tok_ptrs)
+    if (!ptr_ok(p, !tok)) return LIZARD_ERR_INVALID_ARG;
+  if (!ptr_ok(meta_k, d.M == 0) || !ptr_ok(meta_v, d.M == 0) ||
+      !ptr_ok(d_meta_k, d.M == 0) || !ptr_ok(d_meta_v, d.M == 0))
+    return LIZARD_ERR_INVALID_ARG;
+  if (!ptr_ok(h0, true) || !ptr_ok(h_final, true) || !ptr_ok(d_h0, true))
+    return LIZARD_ERR_INVALID_ARG;
+  lizard_status st = shape_supported(d.dk, d.dv);
+  if (st != LIZARD_OK) return st;
+  const size_t need = lizard_fwd_bwd_host_workspace_bytes(dims, W);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return LIZARD_ERR_WORKSPACE;
+  const int W_eff = d.L > 0 && W > d.L ? d.L : W;
+  if (W_eff > kMaxBwdWindow) return LIZARD_ERR_UNSUPPORTED;
+
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  HostPipe* pp = host_pipe();
+  if (!pp) return LIZARD_ERR_CUDA;
+  HostPipe& P = *pp;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int Hs = host_slice_heads(d.H);
+  const int nslices = (d.H + Hs - 1) / Hs;
+  const SliceLayout l = slice_layout(d, Hs, h0 != nullptr, h_final != nullptr, d_h0 != nullptr);
+  unsigned char* base = static_cast<unsigned char*>(workspace);
+  unsigned char* scratch = base + lz::kWsHeader;
+  unsigned char* bufs = scratch + lz::align_up(host_op_scratch(d, W, Hs), 256);
+  const size_t es = elem_size(d.dtype);
+  const size_t rowT = (size_t)d.L * d.dk * es, rowF = (size_t)d.L * d.dk * 4;
+  const size_t rowS = (size_t)d.dk * d.dv * 4;
+  const size_t metaT = (size_t)d.M * d.dk * es, metaF = (size_t)d.M * d.dk * 4;
+  const float scale = resolve_scale(d.scale, d.dk);
+
+  cudaError_t e = cudaMemsetAsync(workspace, 0, lz::kWsHeader, s);
+  // the copy streams start after the work already queued on `stream`
+  if (e == cudaSuccess) e = cudaEventRecord(P.start, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(P.in, P.start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(P.out, P.start, 0);
+  int launches = 0;
+  for (int si = 0; si < nslices && e == cudaSuccess; ++si) {
+    const int b = si & 1, hb = si * Hs, hs = d.H - hb < Hs ? d.H - hb : Hs;
+    unsigned char* buf = bufs + b * l.bytes;
+    auto at = [&](int i) { return static_cast<void*>(buf + l.off[i]); };
+    // copy in (after the compute of the slice that used this buffer two slices ago)
+    if (si >= 2) e = cudaStreamWaitEvent(P.in, P.ev_comp[b], 0);
+    const void* ins[] = {phi_q, phi_k, v, q, k, dy};
+    const int in_ix[] = {SliceLayout::PQ, SliceLayout::PK, SliceLayout::V, SliceLayout::Q,
+                         SliceLayout::K, SliceLayout::DY};
+    for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+      e = copy_heads(at(in_ix[i]), ins[i], d, hb, hs, rowT, true, P.in);
+    if (e == cudaSuccess) e = copy_heads(at(SliceLayout::LG), log_gamma, d, hb, hs, rowF, true, P.in);
+    if (e == cudaSuccess && h0) e = copy_heads(at(SliceLayout::H0), h0, d, hb, hs, rowS, true, P.in);
+    if (e == cudaSuccess && d.M > 0) {
+      e = cudaMemcpyAsync(at(SliceLayout::MK), static_cast<const char*>(meta_k) + hb * metaT,
+                          hs * metaT, cudaMemcpyHostToDevice, P.in);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(at(SliceLayout::MV), static_cast<const char*>(meta_v) + hb * metaT,
+                            hs * metaT, cudaMemcpyHostToDevice, P.in);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(P.ev_in[b], P.in);
+    // compute on `stream` (after this slice's inputs and the copy-out two slices ago)
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, P.ev_in[b], 0);
+    if (e == cudaSuccess && si >= 2) e = cudaStreamWaitEvent(s, P.ev_out[b], 0);
+    if (e == cudaSuccess) {
+      lz::FwdArgs fa{d.B, hs, d.L, d.dk, d.dv, d.M, W_eff, scale, alpha,
+                     at(SliceLayout::PQ), at(SliceLayout::PK), at(SliceLayout::V),
+                     static_cast<const float*>(at(SliceLayout::LG)), at(SliceLayout::Q),
+                     at(SliceLayout::K), d.M ? at(SliceLayout::MK) : nullptr,
+                     d.M ? at(SliceLayout::MV) : nullptr, at(SliceLayout::Y),
+                     h0 ? static_cast<const float*>(at(SliceLayout::H0)) : nullptr,
+                     h_final ? static_cast<float*>(at(SliceLayout::HF)) : nullptr,
+                     static_cast<unsigned*>(workspace), scratch};
+      if (d.L > 0 || h_final) e = dispatch_fwd(fa, d.dtype, s, &launches);
+    }
+    if (e == cudaSuccess) {
+      lz::BwdArgs ba{d.B, hs, d.L, d.dk, d.dv, d.M, W_eff, scale, alpha,
+                     at(SliceLayout::PQ), at(SliceLayout::PK), at(SliceLayout::V),
+                     static_cast<const float*>(at(SliceLayout::LG)), at(SliceLayout::Q),
+                     at(SliceLayout::K), d.M ? at(SliceLayout::MK) : nullptr,
+                     d.M ? at(SliceLayout::MV) : nullptr,
+                     h0 ? static_cast<const float*>(at(SliceLayout::H0)) : nullptr,
+                     at(SliceLayout::DY), at(SliceLayout::DPQ), at(SliceLayout::DPK),
+                     at(SliceLayout::DV), static_cast<float*>(at(SliceLayout::DLG)),
+                     at(SliceLayout::DQ), at(SliceLayout::DK),
+                     d.M ? static_cast<float*>(at(SliceLayout::DMK)) : nullptr,
+                     d.M ? static_cast<float*>(at(SliceLayout::DMV)) : nullptr,
+                     d_h0 ? static_cast<float*>(at(SliceLayout::DH0)) : nullptr,
+                     static_cast<unsigned*>(workspace), scratch, host_op_scratch(d, W, Hs)};
+      e = lz::launch_bwd_simt(ba, d.dtype, s, &launches);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(P.ev_comp[b], s);
+    // copy out
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(P.out, P.ev_comp[b], 0);
+    void* outs[] = {y, d_phi_q, d_phi_k, d_v, d_q, d_k};
+    const int out_ix[] = {SliceLayout::Y, SliceLayout::DPQ, SliceLayout::DPK, SliceLayout::DV,
+                          SliceLayout::DQ, SliceLayout::DK};
+    for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+      e = copy_heads(outs[i], at(out_ix[i]), d, hb, hs, rowT, false, P.out);
+    if (e == cudaSuccess) e = copy_heads(d_log_gamma, at(SliceLayout::DLG), d, hb, hs, rowF, false, P.out);
+    if (e == cudaSuccess && h_final) e = copy_heads(h_final, at(SliceLayout::HF), d, hb, hs, rowS, false, P.out);
+    if (e == cudaSuccess && d_h0) e = copy_heads(d_h0, at(SliceLayout::DH0), d, hb, hs, rowS, false, P.out);
+    if (e == cudaSuccess && d.M > 0) {
+      e = cudaMemcpyAsync(static_cast<char*>(static_cast<void*>(d_meta_k)) + hb * metaF,
+                          at(SliceLayout::DMK), hs * metaF, cudaMemcpyDeviceToHost, P.out);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(static_cast<char*>(static_cast<void*>(d_meta_v)) + hb * metaF,
+                            at(SliceLayout::DMV), hs * metaF, cudaMemcpyDeviceToHost, P.out);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(P.ev_out[b], P.out);
+  }
+  // `stream` covers every copy once it has passed the last copy-out
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, P.ev_out[(nslices - 1) & 1], 0);
+  if (e == cudaSuccess && nslices > 1) e = cudaStreamWaitEvent(s, P.ev_out[nslices & 1], 0);
   g_last_launches = launches;
   return cuda_status(e);
 }

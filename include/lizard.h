@@ -121,6 +121,32 @@ lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* phi_q, const 
                               void* stream);
 
 /*
+ * Forward and backward of one training step with every tensor in HOST memory.
+ *   Arguments as lizard_attn_fwd followed by lizard_attn_bwd (same shapes, types and
+ *   optional pointers), except that phi_q ... dy, y, h_final and all gradients are host
+ *   pointers.  Page-locked (pinned) host memory lets the copies run concurrently with the
+ *   kernels; pageable memory works, with serialised copies.  `workspace` is DEVICE memory
+ *   of lizard_fwd_bwd_host_workspace_bytes(dims, W) bytes.
+ * The heads are processed in slices of ceil(H/8): while slice s is computed on `stream`,
+ * the inputs of slice s+1 are copied in and the results of slice s-1 copied out on two
+ * streams of the library's own (created once per device), ordered after the work already
+ * queued on `stream`; before returning, the call makes `stream` wait for the last copy,
+ * so synchronising `stream` covers the whole step.  Host buffers must stay valid and
+ * unchanged until then.  Results are identical to the two device calls.  Device
+ * conditions are reported through lizard_check_device_errors(workspace, stream).
+ */
+size_t lizard_fwd_bwd_host_workspace_bytes(const lizard_dims* dims, int32_t W);
+lizard_status lizard_attn_fwd_bwd_host(const lizard_dims* dims, const void* phi_q,
+                                       const void* phi_k, const void* v, const float* log_gamma,
+                                       const void* q, const void* k, const void* meta_k,
+                                       const void* meta_v, int32_t W, float alpha,
+                                       const float* h0, const void* dy, void* y, float* h_final,
+                                       void* d_phi_q, void* d_phi_k, void* d_v,
+                                       float* d_log_gamma, void* d_q, void* d_k, float* d_meta_k,
+                                       float* d_meta_v, float* d_h0, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/*
  * One recurrent decode step for N sequences (constant memory per sequence: the state
  * and a W-slot ring; "Lizard", arXiv 2507.09025, Preliminaries: recurrent form).
  *   Token inputs phi_q, phi_k, q, k [N,H,dk] T; v [N,H,dv] T; log_gamma [N,H,dk] fp32.

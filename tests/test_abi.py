@@ -159,9 +159,8 @@ def test_chunk_cumsum_rejects_bad_arguments(lib):
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
-    import importlib
+    # monkeypatch restores the loaded library and its path afterwards
     monkeypatch.setattr(lz, "_lib", None)
     monkeypatch.setattr(lz, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         lz.library()
-    importlib.reload(lz)
