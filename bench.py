@@ -39,12 +39,12 @@ NAMES = ("phi_q", "phi_k", "v", "log_gamma", "q", "k", "meta_k", "meta_v")
 ALGO_BYTES_PER_TOKEN_HEAD = {
     # bytes each kernel must move per (token, head) at d = 128: bf16 rows are 256 B,
     # fp32 rows 512 B; per-chunk states are amortised over the chunk's tokens.
-    "fwd_prep": 2 * 256 + 512 + 2 * 256,      # phi_q, phi_k, log_gamma -> Qt, Kt
+    "fwd_prep": 2 * 256 + 512 + 3 * 256,      # phi_q, phi_k, log_gamma -> Qt, Kt, e^b
     "fwd_scan_tc": 2 * 256 + 256,             # Kt, v -> h (32 KB per 128-token chunk)
     "fwd_chunk_tc": 5 * 256 + 256 + 256,      # Qt, Kt, q, k, v, h -> y
     "fwd_simt": 5 * 256 + 512 + 256,
     "bwd_prep": 2 * 256 + 512 + 3 * 256,      # phi_q, phi_k, log_gamma -> Qt, Kt, e^b
-    "bwd_scan_tc": 4 * 256 + 2 * 256,         # Qt, Kt, v, dy -> h, Gt (2 x 32 KB / 128 tokens)
+    "bwd_scan_tc": 2 * 256 + 256,             # Qt, dy -> Gt (the states come from the forward)
     "bwd_chunk_tc": 4 * 256 + 2 * 256 + 256 + 2 * 256 + 2 * 512,  # + e^b -> d_phi, dv_gla, r
     "bwd_suffix": 2 * 512,                    # r -> d_log_gamma
     "win_bwd_q_tc": 4 * 256 + 256 + 8,        # q, dy, k, v -> d_q, lse, D
@@ -282,7 +282,8 @@ class Problem:
         lz, t, g = self.lz, self.t, self.g
         lz.lizard_attn_bwd(self.dims, *(t[n] for n in NAMES), self.w["W"], 1.0, None, t["dy"],
                            g["d_phi_q"], g["d_phi_k"], g["d_v"], g["d_log_gamma"], g["d_q"],
-                           g["d_k"], g["d_meta_k"], g["d_meta_v"], None, self.ws_b, stream)
+                           g["d_k"], g["d_meta_k"], g["d_meta_v"], None, self.ws_b, stream,
+                           fwd_workspace=self.ws_f)
         self.launches += lz.lizard_last_launch_count()
 
     def step(self, stream=None):

@@ -85,7 +85,7 @@ def library():
             DP, DDP = ctypes.POINTER(lizard_dims), ctypes.POINTER(lizard_decode_dims)
             sig = {
                 "lizard_attn_fwd": (I32, [DP] + [P] * 8 + [I32, F, P, P, P, P, SZ, P]),
-                "lizard_attn_bwd": (I32, [DP] + [P] * 8 + [I32, F] + [P] * 11 + [P, SZ, P]),
+                "lizard_attn_bwd": (I32, [DP] + [P] * 8 + [I32, F] + [P] * 12 + [P, SZ, P]),
                 "lizard_decode_step": (I32, [DDP] + [P] * 8 + [I32, F] + [P] * 5 + [P, SZ, P]),
                 "lizard_chunk_cumsum": (I32, [I32, I32, I32, I32, P, P, P, P]),
                 "lizard_fwd_workspace_bytes": (SZ, [DP, I32]),
@@ -204,14 +204,16 @@ def lizard_attn_fwd(dims: lizard_dims, phi_q, phi_k, v, log_gamma, q, k, meta_k,
 
 def lizard_attn_bwd(dims: lizard_dims, phi_q, phi_k, v, log_gamma, q, k, meta_k, meta_v, W: int,
                     alpha: float, h0, dy, d_phi_q, d_phi_k, d_v, d_log_gamma, d_q, d_k,
-                    d_meta_k, d_meta_v, d_h0, workspace, stream=None):
-    """Backward pass into preallocated gradient tensors."""
+                    d_meta_k, d_meta_v, d_h0, workspace, stream=None, fwd_workspace=None):
+    """Backward pass into preallocated gradient tensors.  ``fwd_workspace``: the workspace
+    of the matching lizard_attn_fwd call, whose chunk features and states are reused."""
     st = library().lizard_attn_bwd(ctypes.byref(dims), _ptr(phi_q), _ptr(phi_k), _ptr(v),
                                    _ptr(log_gamma), _ptr(q), _ptr(k), _ptr(meta_k), _ptr(meta_v),
                                    int(W), float(alpha), _ptr(h0), _ptr(dy), _ptr(d_phi_q),
                                    _ptr(d_phi_k), _ptr(d_v), _ptr(d_log_gamma), _ptr(d_q),
                                    _ptr(d_k), _ptr(d_meta_k), _ptr(d_meta_v), _ptr(d_h0),
-                                   _ptr(workspace), _ws_bytes(workspace), _stream(stream))
+                                   _ptr(fwd_workspace), _ptr(workspace), _ws_bytes(workspace),
+                                   _stream(stream))
     _check(st, "lizard_attn_bwd")
 
 

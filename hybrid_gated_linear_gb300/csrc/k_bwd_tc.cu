@@ -411,6 +411,10 @@ cudaError_t launch_tc(K kernel, const M& maps, const P& p, int grid, int threads
 
 }  // namespace
 
+bool fwd_ctx_usable(int dk, int dv, int L, int W, int M, lizard_dtype dt) {
+  return fwd_chunk_tc_supported(dk, dv, L, W, M, dt);
+}
+
 bool bwd_gla_tc_supported(int dk, int dv, int L, lizard_dtype dt) {
   return dt == LIZARD_BF16 && dk == kD && dv == kD && L > 0 && tma_encode_available();
 }
@@ -425,10 +429,22 @@ cudaError_t launch_bwd_gla_tc(const BwdArgs& a, float* dvacc, unsigned char* ws,
   gla_ws_layout(BH, L, ws, &w);
   cudaError_t e;
 
+  // With the forward's context, its Qt, Kt, e^b, Gamma and chunk states are reused and
+  // only the adjoint scan runs.
+  const bool ctx = a.fwd_ws != nullptr && fwd_ctx_usable(a.dk, a.dv, a.L, a.W, a.M, LIZARD_BF16);
+  if (ctx) {
+    const GlaCtx fc = fwd_chunk_tc_ctx(BH, L, a.fwd_ws);
+    w.qt = fc.qt;
+    w.kt = fc.kt;
+    w.eb = fc.eb;
+    w.gam = fc.gam;
+    w.hs = fc.hs;
+  }
   GlaStatesArgs ga{BH, L, a.pq, a.pk, a.lg, a.v, a.dy, a.h0, nullptr, a.dh0,
                    w.qt, w.kt, w.eb, w.gam, w.hs, w.gs, a.status};
-  if ((e = launch_gla_prep(ga, s, launches)) != cudaSuccess) return e;
-  if ((e = launch_gla_scan(ga, true, s, launches)) != cudaSuccess) return e;
+  if (!ctx && (e = launch_gla_prep(ga, s, launches)) != cudaSuccess) return e;
+  if ((e = launch_gla_scan(ga, ctx ? GlaScan::kAdjoints : GlaScan::kBoth, s, launches)) != cudaSuccess)
+    return e;
 
   const uint64_t bhl = (uint64_t)BH, Ll = (uint64_t)L, zs = (uint64_t)BH * nc;
   ChunkMaps cm;

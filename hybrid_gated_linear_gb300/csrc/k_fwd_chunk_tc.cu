@@ -337,11 +337,8 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
   if (threadIdx.x == 0 && ctl->abort) raise_status(p.status, kDevTimeout);
 }
 
-struct FwdWs {
-  bf16 *qt, *kt;  // [BH][L][128]
-  float* gam;     // [BH][nc][128]
-  bf16* hs;       // [BH][nc][128][128]
-};
+// The workspace is the context the backward can reuse (GlaCtx).
+using FwdWs = GlaCtx;
 
 size_t fwd_ws_layout(int BH, int L, unsigned char* p, FwdWs* w) {
   const size_t nc = (L + kC - 1) / kC;
@@ -354,6 +351,7 @@ size_t fwd_ws_layout(int BH, int L, unsigned char* p, FwdWs* w) {
   FwdWs g;
   g.qt = reinterpret_cast<bf16*>(take((size_t)BH * L * kD * sizeof(bf16)));
   g.kt = reinterpret_cast<bf16*>(take((size_t)BH * L * kD * sizeof(bf16)));
+  g.eb = reinterpret_cast<bf16*>(take((size_t)BH * L * kD * sizeof(bf16)));
   g.gam = reinterpret_cast<float*>(take((size_t)BH * nc * kD * sizeof(float)));
   g.hs = reinterpret_cast<bf16*>(take((size_t)BH * nc * kD * kD * sizeof(bf16)));
   if (w) *w = g;
@@ -381,6 +379,12 @@ bool fwd_chunk_tc_supported(int dk, int dv, int L, int W, int M, lizard_dtype dt
 
 size_t fwd_chunk_tc_workspace(int BH, int L) { return fwd_ws_layout(BH, L, nullptr, nullptr); }
 
+GlaCtx fwd_chunk_tc_ctx(int BH, int L, unsigned char* ws) {
+  GlaCtx c;
+  fwd_ws_layout(BH, L, ws, &c);
+  return c;
+}
+
 cudaError_t launch_fwd_chunk_tc(const FwdArgs& a, unsigned char* ws, cudaStream_t s, int* launches) {
   const int BH = a.B * a.H, L = a.L;
   const int nc = (L + kC - 1) / kC;
@@ -388,9 +392,9 @@ cudaError_t launch_fwd_chunk_tc(const FwdArgs& a, unsigned char* ws, cudaStream_
   fwd_ws_layout(BH, L, ws, &w);
   cudaError_t e;
   GlaStatesArgs ga{BH, L, a.pq, a.pk, a.lg, a.v, nullptr, a.h0, a.hf, nullptr,
-                   w.qt, w.kt, nullptr, w.gam, w.hs, nullptr, a.status};
+                   w.qt, w.kt, w.eb, w.gam, w.hs, nullptr, a.status};
   if ((e = launch_gla_prep(ga, s, launches)) != cudaSuccess) return e;
-  if ((e = launch_gla_scan(ga, false, s, launches)) != cudaSuccess) return e;
+  if ((e = launch_gla_scan(ga, GlaScan::kStates, s, launches)) != cudaSuccess) return e;
 
   const int np = a.W <= 65 ? 1 : 2;
   const uint32_t br = (uint32_t)(kC + 64 * np);

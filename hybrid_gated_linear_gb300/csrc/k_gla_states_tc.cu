@@ -90,14 +90,15 @@ constexpr size_t kScanSmem = kScanBars + 1024 + 1024;
 constexpr int kScanThreads = 6 * 32;
 
 __global__ void __launch_bounds__(kScanThreads, 1)
-scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc, int ndir) {
+scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc, int ndir,
+            int dir0) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   using C = Ctl<S_COUNT>;
   C* ctl = reinterpret_cast<C*>(sm + kScanBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int dir = ndir == 2 ? (blockIdx.x & 1) : 0;
+  const int dir = ndir == 2 ? (blockIdx.x & 1) : dir0;
   const int sl = (blockIdx.x / ndir) % kSlices;
   const int bh = blockIdx.x / (ndir * kSlices);
 
@@ -230,33 +231,41 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
 
 cudaError_t launch_gla_prep(const GlaStatesArgs& a, cudaStream_t s, int* launches) {
   const int nc = (a.L + kC - 1) / kC;
-  trace_begin(a.eb ? "bwd_prep" : "fwd_prep", s);
+  trace_begin(a.dy ? "bwd_prep" : "fwd_prep", s);
   prep_kernel<<<dim3(nc, a.BH), kD, 0, s>>>(a, nc);
   trace_end(s);
   ++*launches;
   return cudaGetLastError();
 }
 
-cudaError_t launch_gla_scan(const GlaStatesArgs& a, bool adjoint, cudaStream_t s, int* launches) {
+cudaError_t launch_gla_scan(const GlaStatesArgs& a, GlaScan which, cudaStream_t s, int* launches) {
   const int nc = (a.L + kC - 1) / kC;
   const uint64_t bhl = (uint64_t)a.BH, Ll = (uint64_t)a.L;
+  const bool states = which != GlaScan::kAdjoints, adjoints = which != GlaScan::kStates;
   ScanMaps m;
-  bool ok = make_tma_map_bf16(&m.x0, a.kt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_tma_map_bf16(&m.y0, a.v, kD, Ll, bhl, kSl, kC, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (adjoint) {
+  bool ok = true;
+  if (states)
+    ok = make_tma_map_bf16(&m.x0, a.kt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_tma_map_bf16(&m.y0, a.v, kD, Ll, bhl, kSl, kC, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (adjoints)
     ok = ok && make_tma_map_bf16(&m.x1, a.qt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_tma_map_bf16(&m.y1, a.dy, kD, Ll, bhl, kSl, kC, CU_TENSOR_MAP_SWIZZLE_64B);
-  } else {
+  if (!ok) return cudaErrorInvalidValue;
+  if (!states) {
+    m.x0 = m.x1;
+    m.y0 = m.y1;
+  }
+  if (!adjoints) {
     m.x1 = m.x0;
     m.y1 = m.y0;
   }
-  if (!ok) return cudaErrorInvalidValue;
-  const int ndir = adjoint ? 2 : 1;
+  const int ndir = states && adjoints ? 2 : 1;
+  const int dir0 = states ? 0 : 1;
   cudaError_t e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kScanSmem);
   if (e != cudaSuccess) return e;
-  trace_begin(adjoint ? "bwd_scan_tc" : "fwd_scan_tc", s);
-  scan_kernel<<<a.BH * kSlices * ndir, kScanThreads, kScanSmem, s>>>(m, a, nc, ndir);
+  trace_begin(adjoints ? "bwd_scan_tc" : "fwd_scan_tc", s);
+  scan_kernel<<<a.BH * kSlices * ndir, kScanThreads, kScanSmem, s>>>(m, a, nc, ndir, dir0);
   trace_end(s);
   ++*launches;
   return cudaGetLastError();

@@ -115,12 +115,18 @@ SliceLayout slice_layout(const lizard_dims& d, int Hs, bool h0, bool hf, bool dh
   return l;
 }
 
-size_t host_op_scratch(const lizard_dims& d, int W, int Hs) {
+// Scratch of the forward (kept for the backward, which reuses it) and of the backward for
+// one slice of Hs heads, without their headers.
+size_t host_fwd_scratch(const lizard_dims& d, int W, int Hs) {
   lizard_dims ds = d;
   ds.H = Hs;
-  const size_t f = lizard_fwd_workspace_bytes(&ds, W), b = lizard_bwd_workspace_bytes(&ds, W);
-  const size_t m = f > b ? f : b;
-  return m > lz::kWsHeader ? m - lz::kWsHeader : 0;
+  return lizard_fwd_workspace_bytes(&ds, W) - lz::kWsHeader;
+}
+
+size_t host_bwd_scratch(const lizard_dims& d, int W, int Hs) {
+  lizard_dims ds = d;
+  ds.H = Hs;
+  return lizard_bwd_workspace_bytes(&ds, W) - lz::kWsHeader;
 }
 
 // Copies heads [h0, h0+hs) of a [B, H, rows] tensor (rows bytes per head) between host and
@@ -269,8 +275,8 @@ lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* phi_q, const 
                               int32_t W, float alpha, const float* h0, const void* dy,
                               void* d_phi_q, void* d_phi_k, void* d_v, float* d_log_gamma,
                               void* d_q, void* d_k, float* d_meta_k, float* d_meta_v,
-                              float* d_h0, void* workspace, size_t workspace_bytes,
-                              void* stream) {
+                              float* d_h0, const void* fwd_workspace, void* workspace,
+                              size_t workspace_bytes, void* stream) {
   g_last_launches = 0;
   if (!dims_ok(dims) || W < 1 || !isfinite(alpha)) return LIZARD_ERR_INVALID_ARG;
   const lizard_dims& d = *dims;
@@ -282,7 +288,9 @@ lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* phi_q, const 
   if (!ptr_ok(meta_k, d.M == 0) || !ptr_ok(meta_v, d.M == 0) ||
       !ptr_ok(d_meta_k, d.M == 0) || !ptr_ok(d_meta_v, d.M == 0))
     return LIZARD_ERR_INVALID_ARG;
-  if (!ptr_ok(h0, true) || !ptr_ok(d_h0, true)) return LIZARD_ERR_INVALID_ARG;
+  if (!ptr_ok(h0, true) || !ptr_ok(d_h0, true) || !ptr_ok(fwd_workspace, true))
+    return LIZARD_ERR_INVALID_ARG;
+  if (fwd_workspace && fwd_workspace == workspace) return LIZARD_ERR_INVALID_ARG;
   lizard_status st = shape_supported(d.dk, d.dv);
   if (st != LIZARD_OK) return st;
   const size_t need = lizard_bwd_workspace_bytes(dims, W);
@@ -316,7 +324,10 @@ lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* phi_q, const 
                 d_phi_q, d_phi_k, d_v, d_log_gamma, d_q, d_k, d_meta_k, d_meta_v, d_h0,
                 static_cast<unsigned*>(workspace),
                 static_cast<unsigned char*>(workspace) + lz::kWsHeader,
-                workspace_bytes - lz::kWsHeader};
+                workspace_bytes - lz::kWsHeader,
+                fwd_workspace ? static_cast<unsigned char*>(const_cast<void*>(fwd_workspace)) +
+                                    lz::kWsHeader
+                              : nullptr};
   int launches = 0;
   e = lz::launch_bwd_simt(a, d.dtype, s, &launches);
   g_last_launches = launches;
@@ -375,7 +386,8 @@ size_t lizard_fwd_bwd_host_workspace_bytes(const lizard_dims* dims, int32_t W) {
   if (!dims_ok(dims) || W < 1 || shape_supported(dims->dk, dims->dv) != LIZARD_OK) return 0;
   const int Hs = host_slice_heads(dims->H);
   const SliceLayout l = slice_layout(*dims, Hs, true, true, true);
-  return lz::kWsHeader + lz::align_up(host_op_scratch(*dims, W, Hs), 256) + 2 * l.bytes;
+  return 2 * lz::kWsHeader + lz::align_up(host_fwd_scratch(*dims, W, Hs), 256) +
+         lz::align_up(host_bwd_scratch(*dims, W, Hs), 256) + 2 * l.bytes;
 }
 
 lizard_status lizard_attn_fwd_bwd_host(const lizard_dims* dims, const void* phi_q,
@@ -416,8 +428,13 @@ lizard_status lizard_attn_fwd_bwd_host(const lizard_dims* dims, const void* phi_
   const int nslices = (d.H + Hs - 1) / Hs;
   const SliceLayout l = slice_layout(d, Hs, h0 != nullptr, h_final != nullptr, d_h0 != nullptr);
   unsigned char* base = static_cast<unsigned char*>(workspace);
-  unsigned char* scratch = base + lz::kWsHeader;
-  unsigned char* bufs = scratch + lz::align_up(host_op_scratch(d, W, Hs), 256);
+  // [status header][forward header + scratch][backward scratch][two slice buffers]; the
+  // forward's header slot only gives its scratch the offset the backward expects.
+  unsigned char* fwd_ws = base + lz::kWsHeader;
+  unsigned char* fscratch = fwd_ws + lz::kWsHeader;
+  unsigned char* bscratch = fscratch + lz::align_up(host_fwd_scratch(d, W, Hs), 256);
+  const size_t bbytes = host_bwd_scratch(d, W, Hs);
+  unsigned char* bufs = bscratch + lz::align_up(bbytes, 256);
   const size_t es = elem_size(d.dtype);
   const size_t rowT = (size_t)d.L * d.dk * es, rowF = (size_t)d.L * d.dk * 4;
   const size_t rowS = (size_t)d.dk * d.dv * 4;
@@ -462,7 +479,7 @@ lizard_status lizard_attn_fwd_bwd_host(const lizard_dims* dims, const void* phi_
                      d.M ? at(SliceLayout::MV) : nullptr, at(SliceLayout::Y),
                      h0 ? static_cast<const float*>(at(SliceLayout::H0)) : nullptr,
                      h_final ? static_cast<float*>(at(SliceLayout::HF)) : nullptr,
-                     static_cast<unsigned*>(workspace), scratch};
+                     static_cast<unsigned*>(workspace), fscratch};
       if (d.L > 0 || h_final) e = dispatch_fwd(fa, d.dtype, s, &launches);
     }
     if (e == cudaSuccess) {
@@ -478,7 +495,7 @@ lizard_status lizard_attn_fwd_bwd_host(const lizard_dims* dims, const void* phi_
                      d.M ? static_cast<float*>(at(SliceLayout::DMK)) : nullptr,
                      d.M ? static_cast<float*>(at(SliceLayout::DMV)) : nullptr,
                      d_h0 ? static_cast<float*>(at(SliceLayout::DH0)) : nullptr,
-                     static_cast<unsigned*>(workspace), scratch, host_op_scratch(d, W, Hs)};
+                     static_cast<unsigned*>(workspace), bscratch, bbytes, fscratch};
       e = lz::launch_bwd_simt(ba, d.dtype, s, &launches);
     }
     if (e == cudaSuccess) e = cudaEventRecord(P.ev_comp[b], s);

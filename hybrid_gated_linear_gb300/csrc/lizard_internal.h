@@ -49,6 +49,7 @@ struct BwdArgs {
   unsigned* status;
   unsigned char* ws;  // workspace after the header
   size_t ws_bytes;
+  unsigned char* fwd_ws;  // forward workspace after its header (reused context) or null
 };
 
 struct DecArgs {
@@ -112,8 +113,19 @@ struct GlaStatesArgs {
   unsigned* status;
 };
 cudaError_t launch_gla_prep(const GlaStatesArgs& a, cudaStream_t s, int* launches);
-// Direction 0 (states) always; direction 1 (scaled adjoints) when `adjoint`.
-cudaError_t launch_gla_scan(const GlaStatesArgs& a, bool adjoint, cudaStream_t s, int* launches);
+// Which scans: the chunk-start states h_c, the scaled adjoints Gt_c, or both.
+enum class GlaScan { kStates, kAdjoints, kBoth };
+cudaError_t launch_gla_scan(const GlaStatesArgs& a, GlaScan which, cudaStream_t s, int* launches);
+
+// What the chunk-parallel forward leaves in its workspace for the backward: Qt, Kt, e^b,
+// Gamma and the chunk-start states h_c (see GlaStatesArgs for the layouts).
+struct GlaCtx {
+  bf16 *qt, *kt, *eb;
+  float* gam;
+  bf16* hs;
+};
+// The context inside a forward workspace (after its header) of B*H units of L tokens.
+GlaCtx fwd_chunk_tc_ctx(int BH, int L, unsigned char* ws);
 
 // Tensor-core backward of the GLA branch (bf16, dk = dv = 128, L > 0): writes d_phi_q,
 // d_phi_k, d_log_gamma, d_h0 and the GLA part of dv (fp32 [B*H][L][128]) to dvacc, using
@@ -122,6 +134,9 @@ bool bwd_gla_tc_supported(int dk, int dv, int L, lizard_dtype dt);
 size_t bwd_gla_tc_workspace(int BH, int L);
 cudaError_t launch_bwd_gla_tc(const BwdArgs& a, float* dvacc, unsigned char* ws, cudaStream_t s,
                               int* launches);
+// True when the forward of these dims used the chunk-parallel tensor-core path, so that its
+// workspace holds a GlaCtx the tensor-core GLA backward can reuse.
+bool fwd_ctx_usable(int dk, int dv, int L, int W, int M, lizard_dtype dt);
 // Tensor-core backward of the window branch (bf16, dk = dv = 128, 1 <= W <= 65, M <= 16,
 // L > 0): writes d_q, d_k, d_v (adding the GLA part from dvacc), d_meta_k, d_meta_v; uses
 // lse2/Dw ([B*H][L] fp32) and mpart (bwd_win_tc_meta_floats) as scratch.

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define LIZARD_ABI_VERSION 1
+#define LIZARD_ABI_VERSION 2
 
 typedef enum lizard_status {
     LIZARD_OK = 0,
@@ -106,6 +106,12 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* phi_q, const 
  *   Outputs: d_phi_q, d_phi_k, d_q, d_k [B,H,L,dk] T; d_v [B,H,L,dv] T (GLA + window);
  *   d_log_gamma [B,H,L,dk] fp32; d_meta_k [H,M,dk], d_meta_v [H,M,dv] fp32, summed over
  *   batch and tokens (NULL when M = 0); d_h0 [B,H,dk,dv] fp32 or NULL.
+ * fwd_workspace: NULL, or the workspace of the lizard_attn_fwd call this backward belongs
+ *   to (same dims and W, same phi_q, phi_k, v, log_gamma and h0, unchanged since).  The
+ *   forward's workspace then holds the chunk features and chunk-start states, which the
+ *   backward reuses instead of recomputing them; a forward that did not leave them (other
+ *   shapes or dtypes) is detected from dims and W and the pointer is then ignored.
+ *   Passing a workspace that does not match these conditions gives wrong gradients.
  * The pages give no backward formulas; this is the exact adjoint of the forward.  The
  * log-gate gradient uses d log_gamma_t = sum_{t'>=t} (phi_q (.) d_phi_q - phi_k (.) d_phi_k)_{t'}
  * (exact because the gate enters only through its cumulative sums).  Deterministic:
@@ -117,8 +123,8 @@ lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* phi_q, const 
                               int32_t W, float alpha, const float* h0, const void* dy,
                               void* d_phi_q, void* d_phi_k, void* d_v, float* d_log_gamma,
                               void* d_q, void* d_k, float* d_meta_k, float* d_meta_v,
-                              float* d_h0, void* workspace, size_t workspace_bytes,
-                              void* stream);
+                              float* d_h0, const void* fwd_workspace, void* workspace,
+                              size_t workspace_bytes, void* stream);
 
 /*
  * Forward and backward of one training step with every tensor in HOST memory.

@@ -118,13 +118,13 @@ def test_bwd_rejects_bad_arguments(lib):
     grads = [P(20 + i) for i in range(8)]
     ws = P(40)
     need = lib.lizard_bwd_workspace_bytes(ctypes.byref(dims), 64)
-    st = lib.lizard_attn_bwd(ctypes.byref(dims), *args, 64, 1.0, None, P(10), *grads, None, ws,
-                             need - 1, None)
+    st = lib.lizard_attn_bwd(ctypes.byref(dims), *args, 64, 1.0, None, P(10), *grads, None, None,
+                             ws, need - 1, None)
     assert st == WORKSPACE
     grads2 = list(grads)
     grads2[1] = grads2[0]  # two outputs alias
-    st = lib.lizard_attn_bwd(ctypes.byref(dims), *args, 64, 1.0, None, P(10), *grads2, None, ws,
-                             need, None)
+    st = lib.lizard_attn_bwd(ctypes.byref(dims), *args, 64, 1.0, None, P(10), *grads2, None, None,
+                             ws, need, None)
     assert st == INVALID
 
 

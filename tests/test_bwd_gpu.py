@@ -89,3 +89,43 @@ def test_bwd_flags_gate_sums_out_of_range():
     lz.lizard_attn_bwd(dims, *(t[n] for n in NAMES), 64, 1.0, None, t["dy"], out[0], out[1],
                        out[2], dlg, dq[0], dq[1], dm[0], dm[1], None, ws)
     assert lz.lizard_check_device_errors(ws) == 5
+
+
+@pytest.mark.parametrize("W", [64, 200])
+def test_bwd_reusing_forward_workspace_is_identical(W):
+    """The backward given the forward's workspace reuses its chunk features and states
+    (tensor-core forward, W = 64) or ignores it (W = 200 runs the CUDA-core forward); the
+    gradients are bitwise those of a backward that recomputes everything."""
+    import torch
+    import hybrid_gated_linear_gb300 as lz
+    from gpu_util import code, host, to_dev
+    B, H, L, d, M = 2, 3, 300, 128, 4
+    x = synth.make_fwd_inputs(B, H, L, d, d, M, "bf16", "bimodal", seed=26, with_dy=True)
+    h0 = (0.1 * np.random.default_rng(27).standard_normal((B, H, d, d))).astype(np.float32)
+    t = to_dev({n: x[n] for n in NAMES + ("dy",)}, "bf16")
+    h0t = torch.from_numpy(h0).cuda()
+    dims = lz.lizard_dims(B, H, L, d, d, M, code("bf16"), 0.0)
+    wf = torch.zeros(max(16, lz.lizard_fwd_workspace_bytes(dims, W)), dtype=torch.uint8, device="cuda")
+    y = torch.empty(B, H, L, d, dtype=torch.bfloat16, device="cuda")
+    lz.lizard_attn_fwd(dims, *(t[n] for n in NAMES), W, 0.9, y, h0t, None, wf)
+
+    def run(fwd_ws):
+        wb = torch.zeros(lz.lizard_bwd_workspace_bytes(dims, W), dtype=torch.uint8, device="cuda")
+        g = {n: torch.empty(B, H, L, d, dtype=torch.bfloat16, device="cuda")
+             for n in ("d_phi_q", "d_phi_k", "d_v", "d_q", "d_k")}
+        g["d_log_gamma"] = torch.empty(B, H, L, d, dtype=torch.float32, device="cuda")
+        g["d_meta_k"] = torch.empty(H, M, d, dtype=torch.float32, device="cuda")
+        g["d_meta_v"] = torch.empty(H, M, d, dtype=torch.float32, device="cuda")
+        g["d_h0"] = torch.empty(B, H, d, d, dtype=torch.float32, device="cuda")
+        lz.lizard_attn_bwd(dims, *(t[n] for n in NAMES), W, 0.9, h0t, t["dy"], g["d_phi_q"],
+                           g["d_phi_k"], g["d_v"], g["d_log_gamma"], g["d_q"], g["d_k"],
+                           g["d_meta_k"], g["d_meta_v"], g["d_h0"], wb, fwd_workspace=fwd_ws)
+        assert lz.lizard_check_device_errors(wb) == 0
+        return {n: host(v) for n, v in g.items()}
+
+    assert lz.lizard_check_device_errors(wf) == 0
+    a, b = run(None), run(wf)
+    for n in a:
+        np.testing.assert_array_equal(a[n], b[n], err_msg=n)
+    ref = oracle.bwd(*(x[n] for n in NAMES), x["dy"], W=W, alpha=0.9, h0=h0, want_dh0=True)
+    _check(b, ref, "bf16", GRADS + ("d_h0",))
