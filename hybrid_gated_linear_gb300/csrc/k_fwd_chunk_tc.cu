@@ -62,6 +62,7 @@ struct FMaps {
 
 struct FParams {
   int H, L, M, W, nc;
+  int ahead;  // CTAs per wave: the tile whose inputs this CTA prefetches into L2
   float scale, alpha;
   unsigned* status;
 };
@@ -124,8 +125,24 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
         tma_load_3d(sm + G::KM, &maps.mk, 0, 0, hh, &ctl->bar[F_LDW]);
         tma_load_3d(sm + G::KM + 2048, &maps.mk, 64, 0, hh, &ctl->bar[F_LDW]);
       }
+      // the V band is loaded only after the GLA products; bring it into L2 now
+      tma_prefetch_l2_3d(&maps.vb, 0, t0 - OFF, bh);
+      tma_prefetch_l2_3d(&maps.vb, 64, t0 - OFF, bh);
       bool ok = true;
-      if (!G::QOWN) {
+      // warm L2 with the inputs of the tile one wave later once this tile's are in
+      const int nb = blockIdx.x + p.ahead;
+      if (nb < gridDim.x && (ok = wait_bar(ctl, F_LDW, 0))) {
+        const int nbh = nb / nc, nt0 = (nb % nc) * kC;
+        for (int x = 0; x < kD; x += 64) {
+          tma_prefetch_l2_3d(&maps.qt, x, nt0, nbh);
+          tma_prefetch_l2_3d(&maps.kt, x, nt0, nbh);
+          tma_prefetch_l2_3d(&maps.hs, x, 0, nb);
+          tma_prefetch_l2_3d(&maps.v, x, nt0, nbh);
+          tma_prefetch_l2_3d(&maps.q, x, nt0, nbh);
+          tma_prefetch_l2_3d(&maps.kb, x, nt0 - OFF, nbh);
+        }
+      }
+      if (ok && !G::QOWN) {
         // the query tile goes where h_c was, once Qt h_c has been computed
         if ((ok = wait_bar(ctl, F_SF, 0))) {
           mbar_arrive_expect_tx(&ctl->bar[F_LDQ2], 32768);
@@ -417,7 +434,7 @@ cudaError_t launch_fwd_chunk_tc(const FwdArgs& a, unsigned char* ws, cudaStream_
     m.mv = m.v;
   }
   if (!ok) return cudaErrorInvalidValue;
-  FParams p{a.H, L, a.M, a.W, nc, a.scale, a.alpha, a.status};
+  FParams p{a.H, L, a.M, a.W, nc, ctas_per_wave(1), a.scale, a.alpha, a.status};
   e = np == 1 ? launch_np<1>(m, p, BH * nc, s) : launch_np<2>(m, p, BH * nc, s);
   ++*launches;
   return e;

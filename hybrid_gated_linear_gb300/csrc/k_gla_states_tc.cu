@@ -13,10 +13,10 @@
 //                         G_{nc-1} = 0,  G_{c-1} = diag(e^Gamma_c) G_c + Qt_c^T dY_c
 //                       stored as bf16 h_c and Gt_c = diag(e^Gamma_c) G_c; h_nc is h_final
 //                       and G_{-1} the adjoint of h0 (fp32).  One CTA per (b, h, 32 dv
-//                       columns, direction): warp 0 streams the chunks by TMA, warp 1
-//                       issues one M=128 N=32 K=128 MMA per chunk into a double-buffered
-//                       TMEM tile, warps 2-5 (thread = state row) run the scan in fp32
-//                       registers.
+//                       columns, direction): warp 0 streams the chunks by TMA through a
+//                       4-deep ring, warp 1 issues one M=128 N=32 K=128 MMA per chunk into
+//                       one of 4 TMEM tiles, warps 2-5 (thread = state row) run the scan
+//                       in fp32 registers.
 #include "lizard_dev.cuh"
 #include "lizard_internal.h"
 #include "tc_pipe.cuh"
@@ -81,17 +81,29 @@ struct ScanMaps {
   CUtensorMap x0, y0, x1, y1;  // direction 0: Kt, V ; direction 1: Qt, dY
 };
 
-enum { S_FULL = 0, S_EMPTY = 2, S_DFULL = 4, S_DFREE = 6, S_DONE = 8, S_COUNT };
 constexpr uint32_t kScanX = kC * kD * 2;          // 32 KB: Kt or Qt tile
 constexpr uint32_t kScanY = kC * kSl * 2;         // 8 KB: V or dY slice
 constexpr uint32_t kScanStage = kScanX + kScanY;  // multiple of 1024
-constexpr uint32_t kScanBars = 2 * kScanStage;
-constexpr size_t kScanSmem = kScanBars + 1024 + 1024;
 constexpr int kScanThreads = 6 * 32;
 
+// kStages chunks in flight per CTA (TMA ring and TMEM buffers): 4 when the grid fits in
+// one wave at one CTA per SM, else 2 so that two CTAs share an SM.
+template <int kStages>
+struct ScanCfg {
+  enum { S_FULL = 0, S_EMPTY = kStages, S_DFULL = 2 * kStages, S_DFREE = 3 * kStages,
+         S_DONE = 4 * kStages, S_COUNT };
+  static constexpr uint32_t kBars = kStages * kScanStage;
+  static constexpr size_t kSmem = kBars + 1024 + 1024;
+};
+
+template <int kStages>
 __global__ void __launch_bounds__(kScanThreads, 1)
 scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc, int ndir,
             int dir0) {
+  using SC = ScanCfg<kStages>;
+  enum { S_FULL = SC::S_FULL, S_EMPTY = SC::S_EMPTY, S_DFULL = SC::S_DFULL,
+         S_DFREE = SC::S_DFREE, S_DONE = SC::S_DONE, S_COUNT = SC::S_COUNT };
+  constexpr uint32_t kScanBars = SC::kBars;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -104,12 +116,12 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S_COUNT; ++i)
-      mbar_init(&ctl->bar[i], (i == S_DFREE || i == S_DFREE + 1) ? 128u : 1u);
+      mbar_init(&ctl->bar[i], (i >= S_DFREE && i < S_DFREE + kStages) ? 128u : 1u);
     ctl->abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&ctl->tmem, 64);
+    tmem_alloc(&ctl->tmem, kStages * kSl);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -121,23 +133,23 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
     if (lane == 0) {
       const CUtensorMap* mx = dir ? &maps.x1 : &maps.x0;
       const CUtensorMap* my = dir ? &maps.y1 : &maps.y0;
-      uint32_t armed0 = 0, armed1 = 0;
+      uint32_t armed[kStages] = {};
       bool ok = true;
       for (int u = 0; u < nc && ok; ++u) {
-        const int c = dir ? nc - 1 - u : u, s = u & 1;
-        if (u >= 2 && !(ok = wait_bar(ctl, S_EMPTY + s, ((u >> 1) - 1) & 1))) break;
+        const int c = dir ? nc - 1 - u : u, s = u % kStages, k = u / kStages;
+        if (k >= 1 && !(ok = wait_bar(ctl, S_EMPTY + s, (k - 1) & 1))) break;
         unsigned char* st = sm + s * kScanStage;
         mbar_arrive_expect_tx(&ctl->bar[S_FULL + s], kScanStage);
         tma_load_3d(st, mx, 0, c * kC, bh, &ctl->bar[S_FULL + s]);
         tma_load_3d(st + kScanX / 2, mx, 64, c * kC, bh, &ctl->bar[S_FULL + s]);
         tma_load_3d(st + kScanX, my, sl * kSl, c * kC, bh, &ctl->bar[S_FULL + s]);
-        if (s) ++armed1;
-        else ++armed0;
+#pragma unroll
+        for (int r = 0; r < kStages; ++r) armed[r] += r == s ? 1u : 0u;
       }
       if (!ok) ctl->abort = 1;
       const uint64_t t0 = globaltimer_ns();
-      drain_bar(ctl, S_FULL, armed0, t0);
-      drain_bar(ctl, S_FULL + 1, armed1, t0);
+#pragma unroll
+      for (int r = 0; r < kStages; ++r) drain_bar(ctl, S_FULL + r, armed[r], t0);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -146,9 +158,9 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
       const uint32_t sbase = smem_u32(sm);
       bool ok = true;
       for (int u = 0; u < nc && ok; ++u) {
-        const int s = u & 1;
-        if (!(ok = wait_bar(ctl, S_FULL + s, (u >> 1) & 1))) break;
-        if (u >= 2 && !(ok = wait_bar(ctl, S_DFREE + s, ((u >> 1) - 1) & 1))) break;
+        const int s = u % kStages, k = u / kStages;
+        if (!(ok = wait_bar(ctl, S_FULL + s, k & 1))) break;
+        if (k >= 1 && !(ok = wait_bar(ctl, S_DFREE + s, (k - 1) & 1))) break;
         tc_fence_after();
         const uint32_t xb = sbase + s * kScanStage, yb = xb + kScanX;
         for (int j = 0; j < kC / 16; ++j)
@@ -183,9 +195,9 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
     bf16* outb = dir ? p.gs : p.hs;
     bool ok = true;
     for (int u = 0; u < nc && ok; ++u) {
-      const int c = dir ? nc - 1 - u : u, s = u & 1;
+      const int c = dir ? nc - 1 - u : u, s = u % kStages;
       const float g = expf(p.gam[((size_t)bh * nc + c) * kD + i]);
-      if (!(ok = wait_bar(ctl, S_DFULL + s, (u >> 1) & 1))) break;
+      if (!(ok = wait_bar(ctl, S_DFULL + s, (u / kStages) & 1))) break;
       tc_fence_after();
       uint32_t d[kSl];
       tmem_ld32(tl + s * kSl, d);
@@ -222,7 +234,7 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
   cta_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 64);
+    tmem_dealloc(tmem, kStages * kSl);
   }
   if (threadIdx.x == 0 && ctl->abort) raise_status(p.status, kDevTimeout);
 }
@@ -261,11 +273,14 @@ cudaError_t launch_gla_scan(const GlaStatesArgs& a, GlaScan which, cudaStream_t 
   }
   const int ndir = states && adjoints ? 2 : 1;
   const int dir0 = states ? 0 : 1;
-  cudaError_t e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kScanSmem);
+  const int grid = a.BH * kSlices * ndir;
+  const bool deep = grid <= ctas_per_wave(1);
+  const size_t smem = deep ? ScanCfg<4>::kSmem : ScanCfg<2>::kSmem;
+  auto kern = deep ? scan_kernel<4> : scan_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   trace_begin(adjoints ? "bwd_scan_tc" : "fwd_scan_tc", s);
-  scan_kernel<<<a.BH * kSlices * ndir, kScanThreads, kScanSmem, s>>>(m, a, nc, ndir, dir0);
+  kern<<<grid, kScanThreads, smem, s>>>(m, a, nc, ndir, dir0);
   trace_end(s);
   ++*launches;
   return cudaGetLastError();
