@@ -124,6 +124,7 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
   cta_sync();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -374,6 +375,7 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
     if (!ok) ctl->abort = 1;
   }
 
+  pdl_trigger();
   tc_fence_before();
   cta_sync();
   if (warp == 1) {
@@ -389,13 +391,18 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kD) suffix_kernel(int L, int nc, float* dlg, const float* rtot) {
   const int c = blockIdx.x, bh = blockIdx.y, i = threadIdx.x;
-  if (c == nc - 1) return;
+  pdl_wait();
+  if (c == nc - 1) {
+    pdl_trigger();
+    return;
+  }
   float carry = 0.f;
   for (int c2 = nc - 1; c2 > c; --c2) carry += rtot[((size_t)bh * nc + c2) * kD + i];
   const int t0 = c * kC, n = min(kC, L - t0);
   float* r = dlg + ((size_t)bh * L + t0) * kD + i;
 #pragma unroll 8
   for (int t = 0; t < n; ++t) r[(size_t)t * kD] += carry;
+  pdl_trigger();
 }
 
 template <typename K, typename M, typename P>
@@ -404,9 +411,9 @@ cudaError_t launch_tc(K kernel, const M& maps, const P& p, int grid, int threads
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   trace_begin(name, s);
-  kernel<<<grid, threads, smem, s>>>(maps, p);
+  e = launch_pdl(kernel, dim3(grid), dim3(threads), smem, s, maps, p);
   trace_end(s);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
@@ -467,10 +474,11 @@ cudaError_t launch_bwd_gla_tc(const BwdArgs& a, float* dvacc, unsigned char* ws,
   if (e != cudaSuccess) return e;
 
   trace_begin("bwd_suffix", s);
-  suffix_kernel<<<dim3(nc, BH), kD, 0, s>>>(L, nc, a.dlg, w.rtot);
+  e = launch_pdl(suffix_kernel, dim3(nc, BH), dim3(kD), 0, s, L, nc, a.dlg,
+                 static_cast<const float*>(w.rtot));
   trace_end(s);
   ++*launches;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace lz

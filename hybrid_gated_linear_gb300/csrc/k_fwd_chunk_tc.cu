@@ -98,6 +98,7 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
   cta_sync();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
+  pdl_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -345,6 +346,7 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
     if (!ok) ctl->abort = 1;
   }
 
+  pdl_trigger();
   tc_fence_before();
   cta_sync();
   if (warp == 1) {
@@ -382,9 +384,9 @@ cudaError_t launch_np(const FMaps& maps, const FParams& p, int grid, cudaStream_
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   trace_begin("fwd_chunk_tc", s);
-  fwd_chunk_kernel<NP><<<grid, kThreads, smem, s>>>(maps, p);
+  e = launch_pdl(fwd_chunk_kernel<NP>, dim3(grid), dim3(kThreads), smem, s, maps, p);
   trace_end(s);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace

@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(kD) prep_kernel(const GlaStatesArgs p, int nc)
   const int c = blockIdx.x, bh = blockIdx.y, i = threadIdx.x;
   const int L = p.L, t0 = c * kC, n = min(kC, L - t0);
   const size_t base = ((size_t)bh * L + t0) * kD + i;
+  pdl_wait();
   const bf16* pq = static_cast<const bf16*>(p.pq) + base;
   const bf16* pk = static_cast<const bf16*>(p.pk) + base;
   const float* lg = p.lg + base;
@@ -72,6 +73,7 @@ __global__ void __launch_bounds__(kD) prep_kernel(const GlaStatesArgs p, int nc)
   p.gam[((size_t)bh * nc + c) * kD + i] = run;
   // e^{+-b} must stay inside the fp32/bf16 range for the factorised form.
   if (big > kMaxLogSum) raise_status(p.status, kDevCheck);
+  pdl_trigger();
 }
 
 // ------------------------------------------------------------------------------------
@@ -128,6 +130,7 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
   cta_sync();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -230,6 +233,7 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
     }
   }
 
+  pdl_trigger();
   tc_fence_before();
   cta_sync();
   if (warp == 1) {
@@ -244,10 +248,10 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
 cudaError_t launch_gla_prep(const GlaStatesArgs& a, cudaStream_t s, int* launches) {
   const int nc = (a.L + kC - 1) / kC;
   trace_begin(a.dy ? "bwd_prep" : "fwd_prep", s);
-  prep_kernel<<<dim3(nc, a.BH), kD, 0, s>>>(a, nc);
+  cudaError_t e = launch_pdl(prep_kernel, dim3(nc, a.BH), dim3(kD), 0, s, a, nc);
   trace_end(s);
   ++*launches;
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_gla_scan(const GlaStatesArgs& a, GlaScan which, cudaStream_t s, int* launches) {
@@ -280,10 +284,10 @@ cudaError_t launch_gla_scan(const GlaStatesArgs& a, GlaScan which, cudaStream_t 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   trace_begin(adjoints ? "bwd_scan_tc" : "fwd_scan_tc", s);
-  kern<<<grid, kScanThreads, smem, s>>>(m, a, nc, ndir, dir0);
+  e = launch_pdl(kern, dim3(grid), dim3(kScanThreads), smem, s, m, a, nc, ndir, dir0);
   trace_end(s);
   ++*launches;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace lz

@@ -94,6 +94,7 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
   cta_sync();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -317,6 +318,7 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
     if (!ok) ctl->abort = 1;
   }
 
+  pdl_trigger();
   tc_fence_before();
   cta_sync();
   if (warp == 1) {
@@ -369,6 +371,7 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
   cta_sync();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -528,6 +531,7 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
     if (!ok) ctl->abort = 1;
   }
 
+  pdl_trigger();
   tc_fence_before();
   cta_sync();
   if (warp == 1) {
@@ -544,6 +548,7 @@ __global__ void __launch_bounds__(256) win_meta_kernel(int B, int H, int M, int 
                                                        float alpha, const float* mpart, float* dmk,
                                                        float* dmv) {
   const int hh = blockIdx.x, m = blockIdx.y, d = threadIdx.x;
+  pdl_wait();
   float s = 0.f;
   for (int b = 0; b < B; ++b) {
     const float* part = mpart + ((size_t)(b * H + hh) * nq) * M * 256 + m * 256 + d;
@@ -559,9 +564,9 @@ cudaError_t launch_tc(K kernel, const Mp& maps, const Params& p, int grid, size_
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   trace_begin(name, s);
-  kernel<<<grid, kThreads, smem, s>>>(maps, p);
+  e = launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, s, maps, p);
   trace_end(s);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
@@ -627,11 +632,11 @@ cudaError_t launch_bwd_win_tc(const BwdArgs& a, const float* dvacc, float* lse2,
   if (e != cudaSuccess) return e;
   if (a.M > 0) {
     trace_begin("win_bwd_meta", s);
-    win_meta_kernel<<<dim3(a.H, a.M), 256, 0, s>>>(a.B, a.H, a.M, nq, a.scale, a.alpha, mpart,
-                                                    a.dmk, a.dmv);
+    e = launch_pdl(win_meta_kernel, dim3(a.H, a.M), dim3(256), 0, s, a.B, a.H, a.M, nq, a.scale,
+                   a.alpha, static_cast<const float*>(mpart), a.dmk, a.dmv);
     trace_end(s);
     ++*launches;
-    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
   }
   return e;
 }

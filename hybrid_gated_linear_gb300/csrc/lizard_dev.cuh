@@ -9,6 +9,16 @@ namespace lz {
 
 using bf16 = __nv_bfloat16;
 
+// Programmatic dependent launch (kernels enqueued with launch_pdl): pdl_wait() blocks until
+// the grid launched before this one on the stream has completed and its memory is
+// visible (a no-op without such a dependency); pdl_trigger() lets the next grid start its
+// CTAs once every CTA of this grid has called it or exited.  Every kernel launched with
+// launch_pdl calls pdl_wait() before it reads anything an earlier kernel wrote.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 template <typename T> __device__ __forceinline__ float ld_f(const T* p);
 template <> __device__ __forceinline__ float ld_f<float>(const float* p) { return *p; }
 template <> __device__ __forceinline__ float ld_f<bf16>(const bf16* p) {

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "lizard.h"
 
 namespace lz {
@@ -79,6 +81,24 @@ bool make_tma_map_bf16(CUtensorMap* m, const void* base, uint64_t dim0, uint64_t
 // Same for fp32 elements.
 bool make_tma_map_f32(CUtensorMap* m, const void* base, uint64_t dim0, uint64_t dim1,
                       uint64_t dim2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw);
+
+// Launches `kernel` on `s` with programmatic stream serialisation, so that its CTAs may
+// start (and run up to pdl_wait) while the previous kernel on the stream drains.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Number of SMs of the current device times `per_sm` (cached per device).
 int ctas_per_wave(int per_sm);
