@@ -58,16 +58,22 @@ ALGO_BYTES_PER_TOKEN_HEAD = {
 # source changed since then reports "traffic": null.
 PROFILED_TRAFFIC = {
     # profiles/ncu_step_kernels_llama3_8b.md
-    "bwd_prep": {"bytes_per_token_head": 1506, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
-                 "sha256": "f45c7cbee44dc30cee745e5d71dd6f87390fddc0727852b9a378a7caa2e47fcf"},
-    "bwd_scan_tc": {"bytes_per_token_head": 1277, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
-                    "sha256": "f45c7cbee44dc30cee745e5d71dd6f87390fddc0727852b9a378a7caa2e47fcf"},
-    "bwd_chunk_tc": {"bytes_per_token_head": 2961, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
-                     "sha256": "f45c7cbee44dc30cee745e5d71dd6f87390fddc0727852b9a378a7caa2e47fcf"},
-    "win_bwd_q_tc": {"bytes_per_token_head": 1167, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
-                     "sha256": "a5ea4645244a74af8f6e137ceee39f30a223edc2c2305b5f2d3f82e318bd1c41"},
-    "win_bwd_k_tc": {"bytes_per_token_head": 1874, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
-                     "sha256": "a5ea4645244a74af8f6e137ceee39f30a223edc2c2305b5f2d3f82e318bd1c41"},
+    "fwd_prep": {"bytes_per_token_head": 1508, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
+                "sha256": "2826c75940ae7f48a4adff9f324de002586116904f98fc86bbdf6b896b71edc6"},
+    "fwd_scan_tc": {"bytes_per_token_head": 542, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
+                   "sha256": "2826c75940ae7f48a4adff9f324de002586116904f98fc86bbdf6b896b71edc6"},
+    "fwd_chunk_tc": {"bytes_per_token_head": 1704, "source": "hybrid_gated_linear_gb300/csrc/k_fwd_chunk_tc.cu",
+                    "sha256": "21f428d924d56bcc371fbd35d5cd97de74ca01f12f23e09c0488733cf9c99f8d"},
+    "bwd_scan_tc": {"bytes_per_token_head": 540, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
+                   "sha256": "2826c75940ae7f48a4adff9f324de002586116904f98fc86bbdf6b896b71edc6"},
+    "bwd_chunk_tc": {"bytes_per_token_head": 3134, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
+                    "sha256": "de1faff4a8637d3c238ae54323079a468051cda31f42a494dde9241a1291ab2d"},
+    "bwd_suffix": {"bytes_per_token_head": 549, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
+                  "sha256": "de1faff4a8637d3c238ae54323079a468051cda31f42a494dde9241a1291ab2d"},
+    "win_bwd_q_tc": {"bytes_per_token_head": 1170, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
+                    "sha256": "80c6456f17c1350e3ef5883ed8e5fc564e6d76f68ce0bb2df629ecff03317e47"},
+    "win_bwd_k_tc": {"bytes_per_token_head": 1876, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
+                    "sha256": "80c6456f17c1350e3ef5883ed8e5fc564e6d76f68ce0bb2df629ecff03317e47"},
 }
 
 DECODE_BYTES_PER_UNIT = 2 * 65536 + 2 * 64 * 128 * 2 + 5 * 256 + 512 + 2 * 256 + 256
