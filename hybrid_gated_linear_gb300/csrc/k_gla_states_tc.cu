@@ -33,44 +33,50 @@ constexpr int kSlices = kD / kSl;
 constexpr float kMaxLogSum = 80.f;  // |chunk-local log-gate sum| beyond which e^{+-b} overflows
 
 // ------------------------------------------------------------------------------------
-// prep: one CTA per (chunk, b*h), thread = key dimension.
+// prep: one CTA per (chunk, b*h) of 64 threads, each owning two adjacent key dimensions
+// (4-byte bf16 pairs, 8-byte log-gate pairs), eight tokens' loads in flight.
 // ------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kD) prep_kernel(const GlaStatesArgs p, int nc) {
-  const int c = blockIdx.x, bh = blockIdx.y, i = threadIdx.x;
+constexpr int kPrepThreads = kD / 2;
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const GlaStatesArgs p, int nc) {
+  const int c = blockIdx.x, bh = blockIdx.y, i2 = threadIdx.x;  // columns 2 i2, 2 i2 + 1
   const int L = p.L, t0 = c * kC, n = min(kC, L - t0);
-  const size_t base = ((size_t)bh * L + t0) * kD + i;
+  const size_t base = ((size_t)bh * L + t0) * (kD / 2) + i2;  // in pairs
   pdl_wait();
-  const bf16* pq = static_cast<const bf16*>(p.pq) + base;
-  const bf16* pk = static_cast<const bf16*>(p.pk) + base;
-  const float* lg = p.lg + base;
-  bf16* qt = p.qt + base;
-  bf16* kt = p.kt + base;
-  bf16* eb = p.eb ? p.eb + base : nullptr;
-  float run = 0.f, big = 0.f;
+  const __nv_bfloat162* pq = reinterpret_cast<const __nv_bfloat162*>(p.pq) + base;
+  const __nv_bfloat162* pk = reinterpret_cast<const __nv_bfloat162*>(p.pk) + base;
+  const float2* lg = reinterpret_cast<const float2*>(p.lg) + base;
+  __nv_bfloat162* qt = reinterpret_cast<__nv_bfloat162*>(p.qt) + base;
+  __nv_bfloat162* kt = reinterpret_cast<__nv_bfloat162*>(p.kt) + base;
+  __nv_bfloat162* eb = p.eb ? reinterpret_cast<__nv_bfloat162*>(p.eb) + base : nullptr;
+  float r0 = 0.f, r1 = 0.f, big = 0.f;
   for (int t8 = 0; t8 < n; t8 += 8) {
-    float lv[8], qv[8], kv[8];
+    float2 lv[8];
+    __nv_bfloat162 qv[8], kv[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const bool ok = t8 + u < n;
-      const size_t o = (size_t)(t8 + u) * kD;
-      lv[u] = ok ? lg[o] : 0.f;
-      qv[u] = ok ? __bfloat162float(pq[o]) : 0.f;
-      kv[u] = ok ? __bfloat162float(pk[o]) : 0.f;
+      const size_t o = (size_t)(t8 + u) * (kD / 2);
+      lv[u] = ok ? lg[o] : make_float2(0.f, 0.f);
+      qv[u] = ok ? pq[o] : __floats2bfloat162_rn(0.f, 0.f);
+      kv[u] = ok ? pk[o] : __floats2bfloat162_rn(0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (t8 + u < n) {
-        run += lv[u];
-        big = fmaxf(big, fabsf(run));
-        const float e = __expf(run);
-        const size_t o = (size_t)(t8 + u) * kD;
-        qt[o] = __float2bfloat16_rn(qv[u] * e);
-        kt[o] = __float2bfloat16_rn(kv[u] * __expf(-run));
-        if (eb) eb[o] = __float2bfloat16_rn(e);
+        r0 += lv[u].x;
+        r1 += lv[u].y;
+        big = fmaxf(big, fmaxf(fabsf(r0), fabsf(r1)));
+        const float e0 = __expf(r0), e1 = __expf(r1);
+        const float2 q = __bfloat1622float2(qv[u]), k = __bfloat1622float2(kv[u]);
+        const size_t o = (size_t)(t8 + u) * (kD / 2);
+        qt[o] = __floats2bfloat162_rn(q.x * e0, q.y * e1);
+        kt[o] = __floats2bfloat162_rn(k.x * __expf(-r0), k.y * __expf(-r1));
+        if (eb) eb[o] = __floats2bfloat162_rn(e0, e1);
       }
     }
   }
-  p.gam[((size_t)bh * nc + c) * kD + i] = run;
+  reinterpret_cast<float2*>(p.gam)[((size_t)bh * nc + c) * (kD / 2) + i2] = make_float2(r0, r1);
   // e^{+-b} must stay inside the fp32/bf16 range for the factorised form.
   if (big > kMaxLogSum) raise_status(p.status, kDevCheck);
   pdl_trigger();
@@ -248,7 +254,7 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
 cudaError_t launch_gla_prep(const GlaStatesArgs& a, cudaStream_t s, int* launches) {
   const int nc = (a.L + kC - 1) / kC;
   trace_begin(a.dy ? "bwd_prep" : "fwd_prep", s);
-  cudaError_t e = launch_pdl(prep_kernel, dim3(nc, a.BH), dim3(kD), 0, s, a, nc);
+  cudaError_t e = launch_pdl(prep_kernel, dim3(nc, a.BH), dim3(kPrepThreads), 0, s, a, nc);
   trace_end(s);
   ++*launches;
   return e;
