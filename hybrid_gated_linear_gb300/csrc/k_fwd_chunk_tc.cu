@@ -239,19 +239,23 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
     if ((ok = wait_bar(ctl, F_SF, 0))) {
       tc_fence_after();
 #pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        uint32_t sv[32];
-        tmem_ld32(tl + G::TS + 32 * g, sv);
+      for (int g2 = 0; g2 < 4; g2 += 2) {
+        uint32_t sv[2][32];
+        tmem_ld32(tl + G::TS + 32 * g2, sv[0]);
+        tmem_ld32(tl + G::TS + 32 * g2 + 32, sv[1]);
         tmem_ld_wait();
-        float v[16];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int gg = 0; gg < 2; ++gg) {
+          float v[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int s = 32 * g + 16 * h + e;
-            v[e] = s <= r ? __uint_as_float(sv[16 * h + e]) : 0.f;
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int s = 32 * (g2 + gg) + 16 * h + e;
+              v[e] = s <= r ? __uint_as_float(sv[gg][16 * h + e]) : 0.f;
+            }
+            store16_bf16(sm + G::KT, kC, r, 32 * (g2 + gg) + 16 * h, v);
           }
-          store16_bf16(sm + G::KT, kC, r, 32 * g + 16 * h, v);
         }
       }
     }
@@ -273,37 +277,55 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
       const int b = 16 * (g_lo + g - nmeta) + e;
       return b >= blo && b <= bhi;
     };
+    // The window's logits are read from TMEM in batches of GB 16-column groups per wait;
+    // with one batch (NP = 1) the exponent pass reuses the registers of the max pass.
+    constexpr int GB = NP == 1 ? 8 : 6;
     float sum = 1.f;
     if (ok && (ok = wait_bar(ctl, F_ZF, 0))) {
       tc_fence_after();
-      float mx = -INFINITY;
-      for (int g = 0; g < ng; ++g) {
-        uint32_t z[16];
-        tmem_ld16(tl + G::TZ + zcol(g), z);
-        tmem_ld_wait();
+      const int nbatch = (ng + GB - 1) / GB;
+      uint32_t z[GB][16];
+      auto load_batch = [&](int b) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          if (vis(g, e)) mx = fmaxf(mx, __uint_as_float(z[e]));
+        for (int k = 0; k < GB; ++k)
+          if (b * GB + k < ng) tmem_ld16(tl + G::TZ + zcol(b * GB + k), z[k]);
+        tmem_ld_wait();
+      };
+      float mx = -INFINITY;
+      for (int b = 0; b < nbatch; ++b) {
+        load_batch(b);
+#pragma unroll
+        for (int k = 0; k < GB; ++k) {
+          if (b * GB + k < ng) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (vis(b * GB + k, e)) mx = fmaxf(mx, __uint_as_float(z[k][e]));
+          }
+        }
       }
       const float mxs = mx * zs;
       sum = 0.f;
-      for (int g = 0; g < ng; ++g) {
-        uint32_t z[16];
-        tmem_ld16(tl + G::TZ + zcol(g), z);
-        tmem_ld_wait();
-        float pv[16];
+      for (int b = 0; b < nbatch; ++b) {
+        if (nbatch > 1) load_batch(b);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float ex = vis(g, e) ? ex2_approx(fmaf(__uint_as_float(z[e]), zs, -mxs)) : 0.f;
-          pv[e] = __bfloat162float(__float2bfloat16_rn(ex));  // the value the MMA sees
-          sum += pv[e];
-        }
-        if (g < nmeta) {
+        for (int k = 0; k < GB; ++k) {
+          const int g = b * GB + k;
+          if (g < ng) {
+            float pv[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            *reinterpret_cast<bf16*>(sm + G::PMT + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(pv[e]);
-        } else {
-          store16_bf16(sm + G::KB, kC, r, 16 * (g_lo + g - nmeta), pv);
+            for (int e = 0; e < 16; ++e) {
+              const float ex = vis(g, e) ? ex2_approx(fmaf(__uint_as_float(z[k][e]), zs, -mxs)) : 0.f;
+              pv[e] = __bfloat162float(__float2bfloat16_rn(ex));  // the value the MMA sees
+              sum += pv[e];
+            }
+            if (g < nmeta) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                *reinterpret_cast<bf16*>(sm + G::PMT + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(pv[e]);
+            } else {
+              store16_bf16(sm + G::KB, kC, r, 16 * (g_lo + g - nmeta), pv);
+            }
+          }
         }
       }
     }
@@ -341,7 +363,7 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
       tma_store_3d(&maps.y, sm + G::YS, 0, t0, bh);
       tma_store_3d(&maps.y, sm + G::YS + 16384, 64, t0, bh);
       bulk_commit();
-      bulk_wait_all();
+      bulk_wait_read();  // shared memory may be released once the stores have read it
     }
     if (!ok) ctl->abort = 1;
   }

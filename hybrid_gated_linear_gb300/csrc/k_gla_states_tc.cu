@@ -203,9 +203,16 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
     }
     bf16* outb = dir ? p.gs : p.hs;
     bool ok = true;
+    // the decay of the next chunk is loaded one step ahead (it sits on the scan's chain)
+    auto gam_of = [&](int u) {
+      const int c = dir ? nc - 1 - u : u;
+      return p.gam[((size_t)bh * nc + c) * kD + i];
+    };
+    float lg_next = nc > 0 ? gam_of(0) : 0.f;
     for (int u = 0; u < nc && ok; ++u) {
       const int c = dir ? nc - 1 - u : u, s = u % kStages;
-      const float g = expf(p.gam[((size_t)bh * nc + c) * kD + i]);
+      const float g = expf(lg_next);
+      if (u + 1 < nc) lg_next = gam_of(u + 1);
       if (!(ok = wait_bar(ctl, S_DFULL + s, (u / kStages) & 1))) break;
       tc_fence_after();
       uint32_t d[kSl];
