@@ -558,6 +558,21 @@ cudaError_t launch_typed(const BwdArgs& a, cudaStream_t s, int* launches) {
   BwdWs w = carve(a.ws, a.B, a.H, a.L, D, D, a.M, tc);
   const int BH = a.B * a.H;
   cudaError_t e;
+  if (tc && bwd_win_tc_supported(D, D, a.L, a.W, a.M, kDt)) {
+    // The query half of the window backward does not depend on the GLA branch: it runs on
+    // a second stream beside the GLA kernels, and the key half waits for both.
+    std::lock_guard<std::mutex> lock(side_stream_lock());
+    SideStream* ss = side_stream();
+    if (!ss) return cudaErrorNotReady;
+    if ((e = cudaEventRecord(ss->fork, s)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ss->stream, ss->fork, 0)) != cudaSuccess) return e;
+    if ((e = launch_bwd_win_q_tc(a, w.dvacc, w.lse, w.Dw, w.mpart, ss->stream, launches)) != cudaSuccess)
+      return e;
+    if ((e = cudaEventRecord(ss->join, ss->stream)) != cudaSuccess) return e;
+    if ((e = launch_bwd_gla_tc(a, w.dvacc, w.gla_tc, s, launches)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(s, ss->join, 0)) != cudaSuccess) return e;
+    return launch_bwd_win_k_tc(a, w.dvacc, w.lse, w.Dw, w.mpart, s, launches);
+  }
   if (tc) {
     if ((e = launch_bwd_gla_tc(a, w.dvacc, w.gla_tc, s, launches)) != cudaSuccess) return e;
   } else {
@@ -571,8 +586,10 @@ cudaError_t launch_typed(const BwdArgs& a, cudaStream_t s, int* launches) {
     ++*launches;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (bwd_win_tc_supported(D, D, a.L, a.W, a.M, kDt))
-    return launch_bwd_win_tc(a, w.dvacc, w.lse, w.Dw, w.mpart, s, launches);
+  if (bwd_win_tc_supported(D, D, a.L, a.W, a.M, kDt)) {
+    if ((e = launch_bwd_win_q_tc(a, w.dvacc, w.lse, w.Dw, w.mpart, s, launches)) != cudaSuccess) return e;
+    return launch_bwd_win_k_tc(a, w.dvacc, w.lse, w.Dw, w.mpart, s, launches);
+  }
   if (a.L > 0) {
     const int zcap = a.M + a.W + 1;
     const size_t smem = (size_t)kWarps * (2 * D + zcap) * sizeof(float);

@@ -580,8 +580,10 @@ size_t bwd_win_tc_meta_floats(int BH, int L, int M) {
   return (size_t)BH * ((L + kB - 1) / kB) * M * 256;
 }
 
-cudaError_t launch_bwd_win_tc(const BwdArgs& a, const float* dvacc, float* lse2, float* Dw,
-                              float* mpart, cudaStream_t s, int* launches) {
+// Both halves build the same maps and parameters; `part` selects the query kernel (0) or
+// the key kernel and the meta reduction (1).
+static cudaError_t launch_win_part(int part, const BwdArgs& a, const float* dvacc, float* lse2,
+                                   float* Dw, float* mpart, cudaStream_t s, int* launches) {
   const int BH = a.B * a.H, L = a.L;
   const int nq = (L + kB - 1) / kB;
   const uint64_t bhl = (uint64_t)BH, Ll = (uint64_t)L;
@@ -624,10 +626,12 @@ cudaError_t launch_bwd_win_tc(const BwdArgs& a, const float* dvacc, float* lse2,
   p.dk = static_cast<bf16*>(a.dk_);
   p.dv = static_cast<bf16*>(a.dvv);
   p.status = a.status;
-  cudaError_t e = launch_tc(win_q_kernel, qm, p, BH * nq, kQSmem, "win_bwd_q_tc", s);
-  ++*launches;
-  if (e != cudaSuccess) return e;
-  e = launch_tc(win_k_kernel, km, p, BH * nq, kKSmem, "win_bwd_k_tc", s);
+  if (part == 0) {
+    const cudaError_t eq = launch_tc(win_q_kernel, qm, p, BH * nq, kQSmem, "win_bwd_q_tc", s);
+    ++*launches;
+    return eq;
+  }
+  cudaError_t e = launch_tc(win_k_kernel, km, p, BH * nq, kKSmem, "win_bwd_k_tc", s);
   ++*launches;
   if (e != cudaSuccess) return e;
   if (a.M > 0) {
@@ -639,6 +643,16 @@ cudaError_t launch_bwd_win_tc(const BwdArgs& a, const float* dvacc, float* lse2,
     if (e == cudaSuccess) e = cudaGetLastError();
   }
   return e;
+}
+
+cudaError_t launch_bwd_win_q_tc(const BwdArgs& a, const float* dvacc, float* lse2, float* Dw,
+                                float* mpart, cudaStream_t s, int* launches) {
+  return launch_win_part(0, a, dvacc, lse2, Dw, mpart, s, launches);
+}
+
+cudaError_t launch_bwd_win_k_tc(const BwdArgs& a, const float* dvacc, float* lse2, float* Dw,
+                                float* mpart, cudaStream_t s, int* launches) {
+  return launch_win_part(1, a, dvacc, lse2, Dw, mpart, s, launches);
 }
 
 }  // namespace lz

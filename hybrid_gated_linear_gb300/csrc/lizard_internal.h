@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <utility>
 
 #include "lizard.h"
@@ -162,8 +163,21 @@ bool fwd_ctx_usable(int dk, int dv, int L, int W, int M, lizard_dtype dt);
 // lse2/Dw ([B*H][L] fp32) and mpart (bwd_win_tc_meta_floats) as scratch.
 bool bwd_win_tc_supported(int dk, int dv, int L, int W, int M, lizard_dtype dt);
 size_t bwd_win_tc_meta_floats(int BH, int L, int M);
-cudaError_t launch_bwd_win_tc(const BwdArgs& a, const float* dvacc, float* lse2, float* Dw,
-                              float* mpart, cudaStream_t s, int* launches);
+// The query half (dq, row statistics, meta partials) and the key half (dk, dv with the GLA
+// part from dvacc, meta gradients); the key half needs the query half's outputs.
+cudaError_t launch_bwd_win_q_tc(const BwdArgs& a, const float* dvacc, float* lse2, float* Dw,
+                                float* mpart, cudaStream_t s, int* launches);
+cudaError_t launch_bwd_win_k_tc(const BwdArgs& a, const float* dvacc, float* lse2, float* Dw,
+                                float* mpart, cudaStream_t s, int* launches);
+
+// A second stream of the current device with a fork and a join event, for work that may
+// run beside the caller's stream inside one call; enqueue under side_stream_lock().
+struct SideStream {
+  cudaStream_t stream;
+  cudaEvent_t fork, join;
+};
+SideStream* side_stream();
+std::mutex& side_stream_lock();
 size_t bwd_simt_workspace(int B, int H, int L, int dk, int dv, int M);
 cudaError_t launch_bwd_simt(const BwdArgs& a, lizard_dtype dt, cudaStream_t s, int* launches);
 cudaError_t launch_decode(const DecArgs& a, lizard_dtype dt, cudaStream_t s, int* launches);

@@ -43,6 +43,27 @@ int ctas_per_wave(int per_sm) {
   return cache[dev] * per_sm;
 }
 
+std::mutex& side_stream_lock() {
+  static std::mutex mu;
+  return mu;
+}
+
+SideStream* side_stream() {
+  static SideStream per_dev[64];
+  static bool ready[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ready[dev]) {
+    SideStream& s = per_dev[dev];
+    if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+    ready[dev] = true;
+  }
+  return &per_dev[dev];
+}
+
 bool tma_encode_available() { return get_encode() != nullptr; }
 
 namespace {
