@@ -60,7 +60,32 @@ cudaError_t dispatch_fwd(const lz::FwdArgs& a, lizard_dtype dt, cudaStream_t s, 
 // ---------------------------------------------------------------------------------------
 // Host-memory forward + backward: head slices pipelined over three streams.
 // ---------------------------------------------------------------------------------------
-int host_slice_heads(int H) { return (H + 7) / 8; }  // at most 8 slices
+int host_slice_heads(int H) { return (H + 7) / 8; }  // the widest slice
+
+// Head slices of the host-memory pipeline: the first and the last hold a quarter of the
+// widest slice, so that the copy-in before the first compute and the compute and copy-out
+// after the last copy-in are short; the slices between hold up to the widest.  Returns
+// the count and fills starts (head of each slice) and the end in starts[count].
+int host_slice_plan(int H, int* starts, int max_slices) {
+  const int Hs = host_slice_heads(H);
+  const int edge = (Hs + 3) / 4;
+  int n = 0, h = 0;
+  if (H > 2 * edge + Hs) {
+    starts[n++] = 0;
+    h = edge;
+    const int mid = H - 2 * edge;
+    const int nmid = (mid + Hs - 1) / Hs;
+    for (int k = 0; k < nmid; ++k) {
+      starts[n++] = h;
+      h += mid / nmid + (k < mid % nmid ? 1 : 0);
+    }
+    starts[n++] = h;
+  } else {
+    for (; h < H && n < max_slices; h += Hs) starts[n++] = h;
+  }
+  starts[n] = H;
+  return n;
+}
 
 struct HostPipe {
   cudaStream_t in = nullptr, out = nullptr;
@@ -425,7 +450,8 @@ lizard_status lizard_attn_fwd_bwd_host(const lizard_dims* dims, const void* phi_
   HostPipe& P = *pp;
   cudaStream_t s = (cudaStream_t)stream;
   const int Hs = host_slice_heads(d.H);
-  const int nslices = (d.H + Hs - 1) / Hs;
+  int starts[64];
+  const int nslices = host_slice_plan(d.H, starts, 62);
   const SliceLayout l = slice_layout(d, Hs, h0 != nullptr, h_final != nullptr, d_h0 != nullptr);
   unsigned char* base = static_cast<unsigned char*>(workspace);
   // [status header][forward header + scratch][backward scratch][two slice buffers]; the
@@ -448,7 +474,7 @@ lizard_status lizard_attn_fwd_bwd_host(const lizard_dims* dims, const void* phi_
   if (e == cudaSuccess) e = cudaStreamWaitEvent(P.out, P.start, 0);
   int launches = 0;
   for (int si = 0; si < nslices && e == cudaSuccess; ++si) {
-    const int b = si & 1, hb = si * Hs, hs = d.H - hb < Hs ? d.H - hb : Hs;
+    const int b = si & 1, hb = starts[si], hs = starts[si + 1] - starts[si];
     unsigned char* buf = bufs + b * l.bytes;
     auto at = [&](int i) { return static_cast<void*>(buf + l.off[i]); };
     // copy in (after the compute of the slice that used this buffer two slices ago)

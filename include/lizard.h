@@ -133,7 +133,8 @@ lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* phi_q, const 
  *   pointers.  Page-locked (pinned) host memory lets the copies run concurrently with the
  *   kernels; pageable memory works, with serialised copies.  `workspace` is DEVICE memory
  *   of lizard_fwd_bwd_host_workspace_bytes(dims, W) bytes.
- * The heads are processed in slices of ceil(H/8): while slice s is computed on `stream`,
+ * The heads are processed in slices of up to ceil(H/8) (the first and the last narrower, to
+ * shorten the pipeline's fill and drain): while slice s is computed on `stream`,
  * the inputs of slice s+1 are copied in and the results of slice s-1 copied out on two
  * streams of the library's own (created once per device), ordered after the work already
  * queued on `stream`; before returning, the call makes `stream` wait for the last copy,
