@@ -24,6 +24,7 @@ __all__ = [
     "lizard_abi_version", "lizard_last_launch_count", "lizard_trace_enable", "lizard_trace_read",
     "lizard_decode_step_noalloc", "LIZARD_NOALLOC_MAX_SEQUENCES",
     "lizard_attn_fwd_bwd_host", "lizard_fwd_bwd_host_workspace_bytes",
+    "lizard_decode_ring_fill", "lizard_state_combine",
     "LIZARD_F32", "LIZARD_BF16", "EXPORTED_SYMBOLS",
 ]
 
@@ -37,6 +38,7 @@ EXPORTED_SYMBOLS = (
     "lizard_workspace_init", "lizard_check_device_errors", "lizard_status_string",
     "lizard_abi_version", "lizard_last_launch_count", "lizard_trace_enable", "lizard_trace_read",
     "lizard_decode_step_noalloc", "lizard_attn_fwd_bwd_host", "lizard_fwd_bwd_host_workspace_bytes",
+    "lizard_decode_ring_fill", "lizard_state_combine",
 )
 
 STATUS_NAMES = {0: "LIZARD_OK", 1: "LIZARD_ERR_INVALID_ARG", 2: "LIZARD_ERR_UNSUPPORTED",
@@ -100,6 +102,8 @@ def library():
                 "lizard_trace_read": (I32, [ctypes.c_char_p, I32, ctypes.POINTER(F), I32]),
                 "lizard_decode_step_noalloc": (I32, [DDP] + [P] * 8 + [I32, F] + [P] * 5 + [P]),
                 "lizard_fwd_bwd_host_workspace_bytes": (SZ, [DP, I32]),
+                "lizard_decode_ring_fill": (I32, [DDP, I32, I32] + [P] * 5 + [P]),
+                "lizard_state_combine": (I32, [I32, I32, I32] + [P] * 6 + [P]),
                 "lizard_attn_fwd_bwd_host": (I32, [DP] + [P] * 8 + [I32, F] + [P] * 13 + [P, SZ, P]),
             }
             for name, (res, args) in sig.items():
@@ -280,3 +284,20 @@ def lizard_attn_fwd_bwd_host(dims: lizard_dims, phi_q, phi_k, v, log_gamma, q, k
         _ptr(d_k), _ptr(d_meta_k), _ptr(d_meta_v), _ptr(d_h0), _ptr(workspace),
         _ws_bytes(workspace), _stream(stream))
     _check(st, "lizard_attn_fwd_bwd_host")
+
+
+def lizard_decode_ring_fill(dims: lizard_decode_dims, L: int, W: int, k, v, k_ring, v_ring, pos,
+                            stream=None):
+    """Fills the decode rings and positions from a prefill's last W keys and values."""
+    st = library().lizard_decode_ring_fill(ctypes.byref(dims), int(L), int(W), _ptr(k), _ptr(v),
+                                           _ptr(k_ring), _ptr(v_ring), _ptr(pos), _stream(stream))
+    _check(st, "lizard_decode_ring_fill")
+
+
+def lizard_state_combine(units: int, dk: int, dv: int, gamma_a, h_a, gamma_b, h_b, gamma_out,
+                         h_out, stream=None):
+    """(gamma_out, h_out) = (gamma_a, h_a) o (gamma_b, h_b): segment a followed by segment b."""
+    st = library().lizard_state_combine(int(units), int(dk), int(dv), _ptr(gamma_a), _ptr(h_a),
+                                        _ptr(gamma_b), _ptr(h_b), _ptr(gamma_out), _ptr(h_out),
+                                        _stream(stream))
+    _check(st, "lizard_state_combine")

@@ -407,6 +407,58 @@ lizard_status lizard_decode_step(const lizard_decode_dims* dims, const void* phi
   return cuda_status(e);
 }
 
+lizard_status lizard_decode_ring_fill(const lizard_decode_dims* dims, int32_t L, int32_t W,
+                                      const void* k, const void* v, void* k_ring, void* v_ring,
+                                      int64_t* pos, void* stream) {
+  g_last_launches = 0;
+  if (!dims || dims->N < 1 || dims->H < 1 || L < 0 || W < 1) return LIZARD_ERR_INVALID_ARG;
+  if (dims->dtype != LIZARD_F32 && dims->dtype != LIZARD_BF16) return LIZARD_ERR_INVALID_ARG;
+  const lizard_status st = shape_supported(dims->dk, dims->dv);
+  if (st != LIZARD_OK) return st;
+  if (!ptr_ok(k, L == 0) || !ptr_ok(v, L == 0) || !ptr_ok(k_ring, false) ||
+      !ptr_ok(v_ring, false) || !ptr_ok(pos, false))
+    return LIZARD_ERR_INVALID_ARG;
+  const size_t es = elem_size(dims->dtype);
+  const size_t nr = (size_t)dims->N * dims->H * W * dims->dk * es;
+  const size_t nt = (size_t)dims->N * dims->H * L * dims->dk * es;
+  if (overlap(k_ring, nr, v_ring, nr) || overlap(k_ring, nr, k, nt) || overlap(k_ring, nr, v, nt) ||
+      overlap(v_ring, nr, k, nt) || overlap(v_ring, nr, v, nt) ||
+      overlap(pos, 8 * (size_t)dims->N, k_ring, nr) || overlap(pos, 8 * (size_t)dims->N, v_ring, nr))
+    return LIZARD_ERR_INVALID_ARG;
+  int launches = 0;
+  const cudaError_t e = lz::launch_ring_fill(dims->N, dims->H, L, W, dims->dk, dims->dv,
+                                             dims->dtype, k, v, k_ring, v_ring, pos,
+                                             (cudaStream_t)stream, &launches);
+  g_last_launches = launches;
+  return cuda_status(e);
+}
+
+lizard_status lizard_state_combine(int32_t units, int32_t dk, int32_t dv, const float* gamma_a,
+                                   const float* h_a, const float* gamma_b, const float* h_b,
+                                   float* gamma_out, float* h_out, void* stream) {
+  g_last_launches = 0;
+  if (units < 0 || dk < 1 || dk > 1024 || dv < 4 || dv > 1024 || dv % 4 != 0)
+    return LIZARD_ERR_INVALID_ARG;
+  const bool any = units > 0;
+  if (!ptr_ok(gamma_a, !any || !gamma_out) || !ptr_ok(h_a, !any) || !ptr_ok(gamma_b, !any) ||
+      !ptr_ok(h_b, !any) || !ptr_ok(gamma_out, true) || !ptr_ok(h_out, !any))
+    return LIZARD_ERR_INVALID_ARG;
+  const size_t ng = (size_t)units * dk * 4, nh = ng * dv;
+  if (overlap(gamma_out, ng, gamma_a, ng) || overlap(gamma_out, ng, gamma_b, ng) ||
+      overlap(gamma_out, ng, h_a, nh) || overlap(gamma_out, ng, h_b, nh) ||
+      overlap(gamma_out, ng, h_out, nh) || overlap(h_out, nh, gamma_a, ng) ||
+      overlap(h_out, nh, gamma_b, ng))
+    return LIZARD_ERR_INVALID_ARG;
+  // h_out may coincide with h_a or h_b exactly (elementwise), not partially
+  if ((overlap(h_out, nh, h_a, nh) && h_out != h_a) || (overlap(h_out, nh, h_b, nh) && h_out != h_b))
+    return LIZARD_ERR_INVALID_ARG;
+  int launches = 0;
+  const cudaError_t e = lz::launch_state_combine(units, dk, dv, gamma_a, h_a, gamma_b, h_b,
+                                                 gamma_out, h_out, (cudaStream_t)stream, &launches);
+  g_last_launches = launches;
+  return cuda_status(e);
+}
+
 size_t lizard_fwd_bwd_host_workspace_bytes(const lizard_dims* dims, int32_t W) {
   if (!dims_ok(dims) || W < 1 || shape_supported(dims->dk, dims->dv) != LIZARD_OK) return 0;
   const int Hs = host_slice_heads(dims->H);

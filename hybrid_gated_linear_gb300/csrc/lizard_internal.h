@@ -181,5 +181,12 @@ std::mutex& side_stream_lock();
 size_t bwd_simt_workspace(int B, int H, int L, int dk, int dv, int M);
 cudaError_t launch_bwd_simt(const BwdArgs& a, lizard_dtype dt, cudaStream_t s, int* launches);
 cudaError_t launch_decode(const DecArgs& a, lizard_dtype dt, cudaStream_t s, int* launches);
+// Segment-state combine and the prefill -> decode ring fill (k_state.cu).
+cudaError_t launch_state_combine(int units, int dk, int dv, const float* ga, const float* ha,
+                                 const float* gb, const float* hb, float* go, float* ho,
+                                 cudaStream_t s, int* launches);
+cudaError_t launch_ring_fill(int N, int H, int L, int W, int dk, int dv, lizard_dtype dt,
+                             const void* k, const void* v, void* kr, void* vr, int64_t* pos,
+                             cudaStream_t s, int* launches);
 
 }  // namespace lz

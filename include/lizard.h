@@ -200,6 +200,36 @@ lizard_status lizard_decode_step_noalloc(const lizard_decode_dims* dims, const v
                                          int64_t* pos, void* y, void* stream);
 
 /*
+ * Prefill -> decode handoff: fills the decode rings after a prefill of L tokens.
+ *   k [N,H,L,dk], v [N,H,L,dv] T: the raw window keys and values of the prefill (device;
+ *   NULL allowed when L = 0).  Out: k_ring [N,H,W,dk], v_ring [N,H,W,dv] T with slot
+ *   t mod W holding token t for t in [max(0, L-W), L) and zeros elsewhere; pos [N] int64
+ *   set to L.  With the state h = h_final of lizard_attn_fwd over the same prefill (its
+ *   [B,H,dk,dv] layout is the decode state's [N,H,dk,dv] with N = B), the next
+ *   lizard_decode_step continues the sequence exactly where the prefill stopped.
+ *   ("Lizard", arXiv 2507.09025, Preliminaries: recurrent form; papernotes.org note,
+ *   关键设计: Anchor Window Attention.)
+ */
+lizard_status lizard_decode_ring_fill(const lizard_decode_dims* dims, int32_t L, int32_t W,
+                                      const void* k, const void* v, void* k_ring, void* v_ring,
+                                      int64_t* pos, void* stream);
+
+/*
+ * Associative combine of segment states for a sequence split ("Lizard", arXiv 2507.09025,
+ * Preliminaries: recurrent form).  A segment with log-gate sum Gamma [dk] and final state
+ * h [dk,dv] from a zero start maps an initial state h0 to diag(e^Gamma) h0 + h, so
+ *   (Gamma_a, h_a) o (Gamma_b, h_b) = (Gamma_a + Gamma_b, diag(e^Gamma_b) h_a + h_b)
+ * for segment a followed by segment b.  units independent pairs; gamma_* [units,dk] fp32,
+ * h_* [units,dk,dv] fp32 (device); dv a multiple of 4; gamma_out may be NULL.  h_out may
+ * be h_a or h_b (in place); gamma_out must not overlap gamma_a or gamma_b.  Segment sums
+ * come from lizard_chunk_cumsum (chunk = segment length) and segment states from
+ * lizard_attn_fwd (h0 = NULL, h_final); the combined state is the h0 of the next segment.
+ */
+lizard_status lizard_state_combine(int32_t units, int32_t dk, int32_t dv, const float* gamma_a,
+                                   const float* h_a, const float* gamma_b, const float* h_b,
+                                   float* gamma_out, float* h_out, void* stream);
+
+/*
  * Chunk-local inclusive cumulative sum of log gamma (the reference point of the
  * log-space reparameterisation; "Lizard", arXiv 2507.09025, Method: cumulative gate
  * products c_t).  log_gamma [units,L,dk] fp32 -> b [units,L,dk] fp32 with

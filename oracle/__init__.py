@@ -178,3 +178,13 @@ def chunk_cumsum(log_gamma, chunk):
     rc = _load().oracle_chunk_cumsum(units, L, dk, int(chunk), _ptr(lg), _ptr(b), _ptr(G))
     _check(rc, "chunk_cumsum")
     return b, G
+
+
+def state_combine(gamma_a, h_a, gamma_b, h_b):
+    """Segment a followed by segment b ("Lizard", arXiv 2507.09025, Preliminaries: the
+    recurrence h_i = diag(gamma_i) h_{i-1} + phi_k_i v_i^T): a segment with log-gate sum
+    Gamma and final state h from a zero start maps h0 to diag(exp(Gamma)) h0 + h, so the
+    pair composes as (Gamma_a + Gamma_b, diag(exp(Gamma_b)) h_a + h_b).  fp64 numpy over
+    [..., dk] and [..., dk, dv]."""
+    ga, ha, gb, hb = (_f64(a) for a in (gamma_a, h_a, gamma_b, h_b))
+    return ga + gb, np.exp(gb)[..., :, None] * ha + hb

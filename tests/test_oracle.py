@@ -355,3 +355,33 @@ def test_generator_is_seeded_and_in_range():
     assert np.all(a["phi_q"] > 0) and np.all(a["phi_k"] > 0)
     assert np.all(a["log_gamma"] < 0)
     assert a["log_gamma"][..., :4].mean() < a["log_gamma"][..., 4:].mean()
+
+
+# --------------------------------------------------------------------------------------
+# Segment-state combine (sequence split)
+# --------------------------------------------------------------------------------------
+def test_state_combine_of_segments_gives_the_full_state_and_is_associative():
+    """Final states of consecutive segments computed from zero, combined left to right,
+    equal the final state of the whole sequence; the combine is associative; a segment
+    started from the combined state of its predecessors reproduces the whole sequence's
+    GLA outputs for its tokens."""
+    B, H, L, dk, dv = 2, 2, 30, 4, 5
+    x = _small(B=B, H=H, L=L, dk=dk, dv=dv, M=2, seed=80, gate="bimodal")
+    full = oracle.fwd(*(x[n] for n in _FD_NAMES), W=3, alpha=0.0, want_state=True)
+    cuts = [0, 7, 19, 30]
+    segs = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        part = {n: (x[n][:, :, a:b] if x[n].ndim == 4 else x[n]) for n in _FD_NAMES}
+        out = oracle.fwd(*(part[n] for n in _FD_NAMES), W=3, alpha=0.0, want_state=True)
+        segs.append((x["log_gamma"][:, :, a:b].astype(np.float64).sum(axis=2), out["h_final"]))
+    g01, h01 = oracle.state_combine(*segs[0], *segs[1])
+    g, h = oracle.state_combine(g01, h01, *segs[2])
+    np.testing.assert_allclose(h, full["h_final"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(g, x["log_gamma"].astype(np.float64).sum(axis=2), rtol=1e-12, atol=1e-13)
+    g12, h12 = oracle.state_combine(*segs[1], *segs[2])
+    g_, h_ = oracle.state_combine(*segs[0], g12, h12)
+    np.testing.assert_allclose(h_, h, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(g_, g, rtol=1e-12, atol=1e-13)
+    part = {n: (x[n][:, :, 19:30] if x[n].ndim == 4 else x[n]) for n in _FD_NAMES}
+    y = oracle.fwd(*(part[n] for n in _FD_NAMES), W=3, alpha=0.0, h0=h01)["y"]
+    np.testing.assert_allclose(y, full["y"][:, :, 19:30], rtol=1e-12, atol=1e-13)
