@@ -28,8 +28,6 @@ using namespace tc;
 
 constexpr int kC = kGlaChunk;
 constexpr int kD = 128;
-constexpr int kSl = 32;  // dv columns per scan CTA
-constexpr int kSlices = kD / kSl;
 constexpr float kMaxLogSum = 80.f;  // |chunk-local log-gate sum| beyond which e^{+-b} overflows
 
 // ------------------------------------------------------------------------------------
@@ -89,29 +87,35 @@ struct ScanMaps {
   CUtensorMap x0, y0, x1, y1;  // direction 0: Kt, V ; direction 1: Qt, dY
 };
 
-constexpr uint32_t kScanX = kC * kD * 2;          // 32 KB: Kt or Qt tile
-constexpr uint32_t kScanY = kC * kSl * 2;         // 8 KB: V or dY slice
-constexpr uint32_t kScanStage = kScanX + kScanY;  // multiple of 1024
+constexpr uint32_t kScanX = kC * kD * 2;  // 32 KB: Kt or Qt tile
 constexpr int kScanThreads = 6 * 32;
 
-// kStages chunks in flight per CTA (TMA ring and TMEM buffers): 4 when the grid fits in
-// one wave at one CTA per SM, else 2 so that two CTAs share an SM.
-template <int kStages>
+// SL value columns per CTA (32, 64 or 128) and kStages chunks in flight (TMA ring and
+// TMEM buffers).  The Y slice (V or dY) is a 64-byte-swizzled 32-column tile when SL = 32
+// and 128-byte-swizzled 64-column blocks otherwise.
+template <int kStages, int SL>
 struct ScanCfg {
   enum { S_FULL = 0, S_EMPTY = kStages, S_DFULL = 2 * kStages, S_DFREE = 3 * kStages,
          S_DONE = 4 * kStages, S_COUNT };
-  static constexpr uint32_t kBars = kStages * kScanStage;
+  static constexpr uint32_t kY = kC * SL * 2;
+  static constexpr uint32_t kStage = kScanX + kY;  // multiple of 1024
+  static constexpr uint32_t kBars = kStages * kStage;
   static constexpr size_t kSmem = kBars + 1024 + 1024;
+  static constexpr uint32_t kTmemCols = kStages * SL <= 32 ? 32 : kStages * SL <= 64 ? 64
+                                      : kStages * SL <= 128 ? 128 : kStages * SL <= 256 ? 256 : 512;
+  static_assert(kStages * SL <= 512, "TMEM budget");
+  static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
-template <int kStages>
+template <int kStages, int SL>
 __global__ void __launch_bounds__(kScanThreads, 1)
 scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc, int ndir,
             int dir0) {
-  using SC = ScanCfg<kStages>;
+  using SC = ScanCfg<kStages, SL>;
   enum { S_FULL = SC::S_FULL, S_EMPTY = SC::S_EMPTY, S_DFULL = SC::S_DFULL,
          S_DFREE = SC::S_DFREE, S_DONE = SC::S_DONE, S_COUNT = SC::S_COUNT };
-  constexpr uint32_t kScanBars = SC::kBars;
+  constexpr int kSlicesT = kD / SL;
+  constexpr uint32_t kScanBars = SC::kBars, kStageB = SC::kStage;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -119,8 +123,8 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
   C* ctl = reinterpret_cast<C*>(sm + kScanBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int dir = ndir == 2 ? (blockIdx.x & 1) : dir0;
-  const int sl = (blockIdx.x / ndir) % kSlices;
-  const int bh = blockIdx.x / (ndir * kSlices);
+  const int sl = (blockIdx.x / ndir) % kSlicesT;
+  const int bh = blockIdx.x / (ndir * kSlicesT);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S_COUNT; ++i)
@@ -129,7 +133,7 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&ctl->tmem, kStages * kSl);
+    tmem_alloc(&ctl->tmem, SC::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -147,11 +151,18 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
       for (int u = 0; u < nc && ok; ++u) {
         const int c = dir ? nc - 1 - u : u, s = u % kStages, k = u / kStages;
         if (k >= 1 && !(ok = wait_bar(ctl, S_EMPTY + s, (k - 1) & 1))) break;
-        unsigned char* st = sm + s * kScanStage;
-        mbar_arrive_expect_tx(&ctl->bar[S_FULL + s], kScanStage);
+        unsigned char* st = sm + s * kStageB;
+        mbar_arrive_expect_tx(&ctl->bar[S_FULL + s], kStageB);
         tma_load_3d(st, mx, 0, c * kC, bh, &ctl->bar[S_FULL + s]);
         tma_load_3d(st + kScanX / 2, mx, 64, c * kC, bh, &ctl->bar[S_FULL + s]);
-        tma_load_3d(st + kScanX, my, sl * kSl, c * kC, bh, &ctl->bar[S_FULL + s]);
+        if (SL == 32) {
+          tma_load_3d(st + kScanX, my, sl * SL, c * kC, bh, &ctl->bar[S_FULL + s]);
+        } else {
+#pragma unroll
+          for (int b64 = 0; b64 < SL / 64; ++b64)
+            tma_load_3d(st + kScanX + b64 * (kC * 128), my, sl * SL + 64 * b64, c * kC, bh,
+                        &ctl->bar[S_FULL + s]);
+        }
 #pragma unroll
         for (int r = 0; r < kStages; ++r) armed[r] += r == s ? 1u : 0u;
       }
@@ -162,8 +173,8 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // D[i][j] = sum_s X[s][i] Y[s][j]: A = X^T (MN-major), B = Y slice (MN-major, 64 B rows)
-      const uint32_t id = idesc_bf16(kD, kSl, true, true);
+      // D[i][j] = sum_s X[s][i] Y[s][j]: A = X^T (MN-major), B = Y slice (MN-major)
+      const uint32_t id = idesc_bf16(kD, SL, true, true);
       const uint32_t sbase = smem_u32(sm);
       bool ok = true;
       for (int u = 0; u < nc && ok; ++u) {
@@ -171,10 +182,12 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
         if (!(ok = wait_bar(ctl, S_FULL + s, k & 1))) break;
         if (k >= 1 && !(ok = wait_bar(ctl, S_DFREE + s, (k - 1) & 1))) break;
         tc_fence_after();
-        const uint32_t xb = sbase + s * kScanStage, yb = xb + kScanX;
-        for (int j = 0; j < kC / 16; ++j)
-          mma_bf16(tmem + s * kSl, desc_mn(xb, kC, j), smem_desc(yb + j * 1024, kC * 64, 512, kSw64),
-                   id, j > 0);
+        const uint32_t xb = sbase + s * kStageB, yb = xb + kScanX;
+        for (int j = 0; j < kC / 16; ++j) {
+          const uint64_t bdesc = SL == 32 ? smem_desc(yb + j * 1024, kC * 64, 512, kSw64)
+                                          : desc_mn(yb, kC, j);
+          mma_bf16(tmem + s * SL, desc_mn(xb, kC, j), bdesc, id, j > 0);
+        }
         mma_commit(&ctl->bar[S_EMPTY + s]);
         mma_commit(&ctl->bar[S_DFULL + s]);
       }
@@ -186,11 +199,11 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
     const int qw = warp & 3;
     const int i = qw * 32 + lane;  // state row = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(qw * 32) << 16);
-    float x[kSl];
+    float x[SL];
     if (dir == 0 && p.h0) {
-      const float4* src = reinterpret_cast<const float4*>(p.h0 + ((size_t)bh * kD + i) * kD + sl * kSl);
+      const float4* src = reinterpret_cast<const float4*>(p.h0 + ((size_t)bh * kD + i) * kD + sl * SL);
 #pragma unroll
-      for (int k = 0; k < kSl / 4; ++k) {
+      for (int k = 0; k < SL / 4; ++k) {
         const float4 v = src[k];
         x[4 * k] = v.x;
         x[4 * k + 1] = v.y;
@@ -199,7 +212,7 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
       }
     } else {
 #pragma unroll
-      for (int k = 0; k < kSl; ++k) x[k] = 0.f;
+      for (int k = 0; k < SL; ++k) x[k] = 0.f;
     }
     bf16* outb = dir ? p.gs : p.hs;
     bool ok = true;
@@ -215,34 +228,39 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
       if (u + 1 < nc) lg_next = gam_of(u + 1);
       if (!(ok = wait_bar(ctl, S_DFULL + s, (u / kStages) & 1))) break;
       tc_fence_after();
-      uint32_t d[kSl];
-      tmem_ld32(tl + s * kSl, d);
-      tmem_ld_wait();
+      uint4* dst = reinterpret_cast<uint4*>(outb + (((size_t)bh * nc + c) * kD + i) * kD + sl * SL);
+#pragma unroll
+      for (int g32 = 0; g32 < SL / 32; ++g32) {
+        uint32_t d[32];
+        tmem_ld32(tl + s * SL + 32 * g32, d);
+        tmem_ld_wait();
+        float* xs = x + 32 * g32;
+        if (dir) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) xs[k] *= g;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          dst[4 * g32 + k] =
+              make_uint4(pack_bf16x2(xs[8 * k], xs[8 * k + 1]), pack_bf16x2(xs[8 * k + 2], xs[8 * k + 3]),
+                         pack_bf16x2(xs[8 * k + 4], xs[8 * k + 5]), pack_bf16x2(xs[8 * k + 6], xs[8 * k + 7]));
+        if (dir) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) xs[k] += __uint_as_float(d[k]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) xs[k] = g * (xs[k] + __uint_as_float(d[k]));
+        }
+      }
       tc_fence_before();
       mbar_arrive(&ctl->bar[S_DFREE + s]);
-      if (dir) {
-#pragma unroll
-        for (int k = 0; k < kSl; ++k) x[k] *= g;
-      }
-      uint4* dst = reinterpret_cast<uint4*>(outb + (((size_t)bh * nc + c) * kD + i) * kD + sl * kSl);
-#pragma unroll
-      for (int k = 0; k < kSl / 8; ++k)
-        dst[k] = make_uint4(pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
-                            pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
-      if (dir) {
-#pragma unroll
-        for (int k = 0; k < kSl; ++k) x[k] += __uint_as_float(d[k]);
-      } else {
-#pragma unroll
-        for (int k = 0; k < kSl; ++k) x[k] = g * (x[k] + __uint_as_float(d[k]));
-      }
     }
     if (!ok) ctl->abort = 1;
     float* fin = dir ? p.dh0 : p.hf;
     if (ok && fin) {
-      float4* dst = reinterpret_cast<float4*>(fin + ((size_t)bh * kD + i) * kD + sl * kSl);
+      float4* dst = reinterpret_cast<float4*>(fin + ((size_t)bh * kD + i) * kD + sl * SL);
 #pragma unroll
-      for (int k = 0; k < kSl / 4; ++k) dst[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+      for (int k = 0; k < SL / 4; ++k) dst[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
     }
   }
 
@@ -251,7 +269,7 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
   cta_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kStages * kSl);
+    tmem_dealloc(tmem, SC::kTmemCols);
   }
   if (threadIdx.x == 0 && ctl->abort) raise_status(p.status, kDevTimeout);
 }
@@ -267,18 +285,20 @@ cudaError_t launch_gla_prep(const GlaStatesArgs& a, cudaStream_t s, int* launche
   return e;
 }
 
-cudaError_t launch_gla_scan(const GlaStatesArgs& a, GlaScan which, cudaStream_t s, int* launches) {
-  const int nc = (a.L + kC - 1) / kC;
+template <int kStages, int SL>
+cudaError_t scan_variant(const GlaStatesArgs& a, bool states, bool adjoints, int nc, cudaStream_t s) {
+  using SC = ScanCfg<kStages, SL>;
   const uint64_t bhl = (uint64_t)a.BH, Ll = (uint64_t)a.L;
-  const bool states = which != GlaScan::kAdjoints, adjoints = which != GlaScan::kStates;
+  const uint32_t ybox = SL == 32 ? 32 : 64;
+  const CUtensorMapSwizzle ysw = SL == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   ScanMaps m;
   bool ok = true;
   if (states)
     ok = make_tma_map_bf16(&m.x0, a.kt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         make_tma_map_bf16(&m.y0, a.v, kD, Ll, bhl, kSl, kC, CU_TENSOR_MAP_SWIZZLE_64B);
+         make_tma_map_bf16(&m.y0, a.v, kD, Ll, bhl, ybox, kC, ysw);
   if (adjoints)
     ok = ok && make_tma_map_bf16(&m.x1, a.qt, kD, Ll, bhl, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         make_tma_map_bf16(&m.y1, a.dy, kD, Ll, bhl, kSl, kC, CU_TENSOR_MAP_SWIZZLE_64B);
+         make_tma_map_bf16(&m.y1, a.dy, kD, Ll, bhl, ybox, kC, ysw);
   if (!ok) return cudaErrorInvalidValue;
   if (!states) {
     m.x0 = m.x1;
@@ -290,14 +310,24 @@ cudaError_t launch_gla_scan(const GlaStatesArgs& a, GlaScan which, cudaStream_t 
   }
   const int ndir = states && adjoints ? 2 : 1;
   const int dir0 = states ? 0 : 1;
-  const int grid = a.BH * kSlices * ndir;
-  const bool deep = grid <= ctas_per_wave(1);
-  const size_t smem = deep ? ScanCfg<4>::kSmem : ScanCfg<2>::kSmem;
-  auto kern = deep ? scan_kernel<4> : scan_kernel<2>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const int grid = a.BH * (kD / SL) * ndir;
+  auto kern = scan_kernel<kStages, SL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SC::kSmem);
   if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(grid), dim3(kScanThreads), SC::kSmem, s, m, a, nc, ndir, dir0);
+}
+
+cudaError_t launch_gla_scan(const GlaStatesArgs& a, GlaScan which, cudaStream_t s, int* launches) {
+  const int nc = (a.L + kC - 1) / kC;
+  const bool states = which != GlaScan::kAdjoints, adjoints = which != GlaScan::kStates;
+  const int ndir = states && adjoints ? 2 : 1;
+  // 32 value columns per CTA: measured against 64 and 128 (which read each Kt/Qt tile fewer
+  // times), the narrow slice keeps the per-chunk chain of every CTA shortest.
   trace_begin(adjoints ? "bwd_scan_tc" : "fwd_scan_tc", s);
-  e = launch_pdl(kern, dim3(grid), dim3(kScanThreads), smem, s, m, a, nc, ndir, dir0);
+  const cudaError_t e = a.BH * 4 * ndir <= ctas_per_wave(1)
+                            ? scan_variant<4, 32>(a, states, adjoints, nc, s)
+                            : scan_variant<2, 32>(a, states, adjoints, nc, s);
   trace_end(s);
   ++*launches;
   return e;
