@@ -3,7 +3,7 @@
 Every function below has the name of a C entry point and only marshals arguments:
 tensors become device pointers, the stream becomes a ``cudaStream_t``, and a non-OK
 status raises :class:`LizardError`.  All arithmetic runs in the library's CUDA kernels;
-there is no Python or CPU fallback.  Call :func:`build` (or ``__graft_entry__.build``)
+there is no Python or CPU fallback.  Call :func:`build`
 once to compile ``_build/liblizard.so``; importing works without it, but every call
 raises until the library is present.
 """

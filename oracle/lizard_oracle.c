@@ -16,7 +16,7 @@
  *        Window formula softmax([q_i^T T ; q_i^T k_{i-W:i}]) [V_T ; v_{i-W:i}];
  *        section "整体框架": the two branch outputs are summed with a weight.
  *
- * Readings taken where the pages are silent (each one also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - the window holds W keys including the query's own token: j in [max(0,i-W+1), i];
  *   - meta keys/values are per head, shared over the batch, always visible;
  *   - softmax logits are scale * <q, key> (scale passed in, normally 1/sqrt(dk));
