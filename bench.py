@@ -52,6 +52,8 @@ ALGO_BYTES_PER_TOKEN_HEAD = {
     "gla_bwd_simt": 4 * 256 + 512 + 2 * 256 + 512,
     "win_bwd_query": 4 * 256 + 256,
     "win_bwd_key": 4 * 256 + 2 * 256,
+    "fmap_fwd_tc": 2 * 256,                   # x -> phi (feature map, D = 128, 2F = 128)
+    "fmap_bwd_tc": 3 * 256,                   # x, d_phi -> d_x
 }
 # DRAM bytes (read + write) per (token, head) from the ncu captures summarised under
 # profiles/, each with the sha256 of the kernel source it was taken on: a kernel whose
@@ -438,6 +440,55 @@ def _decode_part(dev, stream, peaks, steps=64):
                          "algorithmic_bytes_per_step": DECODE_BYTES_PER_UNIT * units}}
 
 
+def _fmap_part(dev, peaks, flush, reps=20):
+    """Hedgehog feature map on the attention workload's shape (B=1, H=32, L=4096, D=128
+    input features, F=64, bf16): forward and backward timed separately with CUDA events,
+    L2 flushed before each launch.  Algorithmic bytes per (token, head): forward reads x
+    and writes phi (2 x 256 B); backward reads x and d_phi and writes d_x (3 x 256 B); W
+    and dW are counted once per launch."""
+    import torch
+
+    import hybrid_gated_linear_gb300 as lz
+    import synth
+    B, H, L, D, F = 1, 32, 4096, 128, 64
+    x = synth.make_fmap_inputs(B, H, L, D, F, "bf16", seed=1005, with_dphi=True)
+    bf = torch.bfloat16
+    X, Wt, dp = (torch.from_numpy(x[n]).to(dev).to(bf) for n in ("x", "w", "d_phi"))
+    dims = lz.lizard_fmap_dims(B, H, L, D, F, lz.LIZARD_BF16)
+    ws = torch.zeros(lz.lizard_feature_map_workspace_bytes(dims, True), dtype=torch.uint8, device=dev)
+    phi = torch.empty(B, H, L, 2 * F, dtype=bf, device=dev)
+    dx = torch.empty(B, H, L, D, dtype=bf, device=dev)
+    dw = torch.empty(H, D, F, dtype=torch.float32, device=dev)
+    fwd = lambda: lz.lizard_feature_map_fwd(dims, X, Wt, phi, ws)
+    bwd = lambda: lz.lizard_feature_map_bwd(dims, X, Wt, dp, dx, dw, ws)
+    out = {"workload": f"Hedgehog feature map B={B}, H={H}, L={L}, D={D}, F={F}, bf16 "
+                       "(tensor-core path); L2 flushed before each launch"}
+    units = B * H * L
+    for name, fn, per_unit, extra in (("fwd", fwd, 2 * 256, H * D * F * 2),
+                                      ("bwd", bwd, 3 * 256, H * D * F * (2 + 4))):
+        for _ in range(3):
+            fn()
+        times = []
+        for _ in range(reps):
+            flush()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = statistics.mean(times)
+        nbytes = per_unit * units + extra
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"us": ms * 1e3, "algorithmic_bytes": nbytes,
+                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                                  "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}}
+    if lz.lizard_check_device_errors(ws) != 0:
+        raise RuntimeError("feature map: device status word set")
+    return out
+
+
 def _e2e(prob, steps, dev):
     """The same fwd+bwd step through the host-memory entry point lizard_attn_fwd_bwd_host:
     pinned host buffers, every input copied to the device and y plus every gradient
@@ -577,6 +628,10 @@ def run_ours(args):
         parts["decode"] = _decode_part(dev, stream, peaks)
     except Exception as e:  # reported, never hidden
         parts["decode"] = {"error": repr(e)}
+    try:
+        parts["feature_map"] = _fmap_part(dev, peaks, flush)
+    except Exception as e:  # reported, never hidden
+        parts["feature_map"] = {"error": repr(e)}
     e2e_ms, h2d, d2h = _e2e(prob, max(3, args.steps // 2), dev)
     e2e_ms = _max_over_ranks(e2e_ms, world, dev)
 

@@ -24,7 +24,8 @@ __all__ = [
     "lizard_abi_version", "lizard_last_launch_count", "lizard_trace_enable", "lizard_trace_read",
     "lizard_decode_step_noalloc", "LIZARD_NOALLOC_MAX_SEQUENCES",
     "lizard_attn_fwd_bwd_host", "lizard_fwd_bwd_host_workspace_bytes",
-    "lizard_decode_ring_fill", "lizard_state_combine",
+    "lizard_decode_ring_fill", "lizard_state_combine", "lizard_fmap_dims",
+    "lizard_feature_map_fwd", "lizard_feature_map_bwd", "lizard_feature_map_workspace_bytes",
     "LIZARD_F32", "LIZARD_BF16", "EXPORTED_SYMBOLS",
 ]
 
@@ -38,7 +39,8 @@ EXPORTED_SYMBOLS = (
     "lizard_workspace_init", "lizard_check_device_errors", "lizard_status_string",
     "lizard_abi_version", "lizard_last_launch_count", "lizard_trace_enable", "lizard_trace_read",
     "lizard_decode_step_noalloc", "lizard_attn_fwd_bwd_host", "lizard_fwd_bwd_host_workspace_bytes",
-    "lizard_decode_ring_fill", "lizard_state_combine",
+    "lizard_decode_ring_fill", "lizard_state_combine", "lizard_feature_map_fwd",
+    "lizard_feature_map_bwd", "lizard_feature_map_workspace_bytes",
 )
 
 STATUS_NAMES = {0: "LIZARD_OK", 1: "LIZARD_ERR_INVALID_ARG", 2: "LIZARD_ERR_UNSUPPORTED",
@@ -65,6 +67,11 @@ class lizard_decode_dims(ctypes.Structure):
                 ("scale", ctypes.c_float)]
 
 
+class lizard_fmap_dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("L", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("F", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -85,6 +92,7 @@ def library():
             lib = ctypes.CDLL(LIB_PATH)
             P, I32, F, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
             DP, DDP = ctypes.POINTER(lizard_dims), ctypes.POINTER(lizard_decode_dims)
+            FMP = ctypes.POINTER(lizard_fmap_dims)
             sig = {
                 "lizard_attn_fwd": (I32, [DP] + [P] * 8 + [I32, F, P, P, P, P, SZ, P]),
                 "lizard_attn_bwd": (I32, [DP] + [P] * 8 + [I32, F] + [P] * 12 + [P, SZ, P]),
@@ -104,6 +112,9 @@ def library():
                 "lizard_fwd_bwd_host_workspace_bytes": (SZ, [DP, I32]),
                 "lizard_decode_ring_fill": (I32, [DDP, I32, I32] + [P] * 5 + [P]),
                 "lizard_state_combine": (I32, [I32, I32, I32] + [P] * 6 + [P]),
+                "lizard_feature_map_workspace_bytes": (SZ, [FMP, I32]),
+                "lizard_feature_map_fwd": (I32, [FMP, P, P, P, P, SZ, P]),
+                "lizard_feature_map_bwd": (I32, [FMP, P, P, P, P, P, P, SZ, P]),
                 "lizard_attn_fwd_bwd_host": (I32, [DP] + [P] * 8 + [I32, F] + [P] * 13 + [P, SZ, P]),
             }
             for name, (res, args) in sig.items():
@@ -301,3 +312,22 @@ def lizard_state_combine(units: int, dk: int, dv: int, gamma_a, h_a, gamma_b, h_
                                         _ptr(gamma_b), _ptr(h_b), _ptr(gamma_out), _ptr(h_out),
                                         _stream(stream))
     _check(st, "lizard_state_combine")
+
+
+def lizard_feature_map_workspace_bytes(dims: lizard_fmap_dims, is_bwd: bool) -> int:
+    return int(library().lizard_feature_map_workspace_bytes(ctypes.byref(dims), int(bool(is_bwd))))
+
+
+def lizard_feature_map_fwd(dims: lizard_fmap_dims, x, w, phi, workspace, stream=None):
+    """phi = [exp(x W), exp(-x W)] per head (Hedgehog feature map)."""
+    st = library().lizard_feature_map_fwd(ctypes.byref(dims), _ptr(x), _ptr(w), _ptr(phi),
+                                          _ptr(workspace), _ws_bytes(workspace), _stream(stream))
+    _check(st, "lizard_feature_map_fwd")
+
+
+def lizard_feature_map_bwd(dims: lizard_fmap_dims, x, w, d_phi, d_x, d_w, workspace, stream=None):
+    """Gradients of the feature map: d_x [B,H,L,D] and d_w [H,D,F] (fp32)."""
+    st = library().lizard_feature_map_bwd(ctypes.byref(dims), _ptr(x), _ptr(w), _ptr(d_phi),
+                                          _ptr(d_x), _ptr(d_w), _ptr(workspace), _ws_bytes(workspace),
+                                          _stream(stream))
+    _check(st, "lizard_feature_map_bwd")

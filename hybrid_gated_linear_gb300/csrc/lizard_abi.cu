@@ -459,6 +459,78 @@ lizard_status lizard_state_combine(int32_t units, int32_t dk, int32_t dv, const 
   return cuda_status(e);
 }
 
+namespace {
+bool fmap_dims_ok(const lizard_fmap_dims* d) {
+  if (!d || d->B < 1 || d->H < 1 || d->L < 0) return false;
+  if (d->dtype != LIZARD_F32 && d->dtype != LIZARD_BF16) return false;
+  if ((long long)d->B * d->H > 65535LL) return false;
+  if ((long long)d->B * d->H * (long long)d->L > (1LL << 40)) return false;
+  return lz::fmap_simt_supported(d->D, d->F);
+}
+}  // namespace
+
+size_t lizard_feature_map_workspace_bytes(const lizard_fmap_dims* dims, int32_t is_bwd) {
+  if (!fmap_dims_ok(dims)) return 0;
+  if (!is_bwd) return lz::kWsHeader;
+  return lz::kWsHeader + lz::fmap_bwd_workspace(dims->B, dims->H, dims->L, dims->D, dims->F,
+                                               dims->dtype);
+}
+
+lizard_status lizard_feature_map_fwd(const lizard_fmap_dims* dims, const void* x, const void* w,
+                                     void* phi, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  g_last_launches = 0;
+  if (!fmap_dims_ok(dims)) return LIZARD_ERR_INVALID_ARG;
+  const lizard_fmap_dims& d = *dims;
+  const bool tok = d.L > 0;
+  if (!ptr_ok(x, !tok) || !ptr_ok(w, false) || !ptr_ok(phi, !tok)) return LIZARD_ERR_INVALID_ARG;
+  const size_t need = lizard_feature_map_workspace_bytes(dims, 0);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return LIZARD_ERR_WORKSPACE;
+  const size_t es = elem_size(d.dtype), rows = (size_t)d.B * d.H * d.L;
+  const size_t nphi = rows * 2 * d.F * es;
+  if (overlap(phi, nphi, x, rows * d.D * es) || overlap(phi, nphi, w, (size_t)d.H * d.D * d.F * es) ||
+      overlap(phi, nphi, workspace, workspace_bytes))
+    return LIZARD_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemsetAsync(workspace, 0, lz::kWsHeader, s) != cudaSuccess) return LIZARD_ERR_CUDA;
+  int launches = 0;
+  const cudaError_t e = lz::launch_fmap_fwd(d.B, d.H, d.L, d.D, d.F, d.dtype, x, w, phi,
+                                            static_cast<unsigned*>(workspace), s, &launches);
+  g_last_launches = launches;
+  return cuda_status(e);
+}
+
+lizard_status lizard_feature_map_bwd(const lizard_fmap_dims* dims, const void* x, const void* w,
+                                     const void* d_phi, void* d_x, float* d_w, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  g_last_launches = 0;
+  if (!fmap_dims_ok(dims)) return LIZARD_ERR_INVALID_ARG;
+  const lizard_fmap_dims& d = *dims;
+  const bool tok = d.L > 0;
+  if (!ptr_ok(x, !tok) || !ptr_ok(w, false) || !ptr_ok(d_phi, !tok) || !ptr_ok(d_x, !tok) ||
+      !ptr_ok(d_w, false))
+    return LIZARD_ERR_INVALID_ARG;
+  const size_t need = lizard_feature_map_workspace_bytes(dims, 1);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return LIZARD_ERR_WORKSPACE;
+  const size_t es = elem_size(d.dtype), rows = (size_t)d.B * d.H * d.L;
+  const size_t nx = rows * d.D * es, nw = (size_t)d.H * d.D * d.F * es, np = rows * 2 * d.F * es;
+  const size_t ndw = (size_t)d.H * d.D * d.F * sizeof(float);
+  const struct { const void* p; size_t n; } ins[] = {{x, nx}, {w, nw}, {d_phi, np},
+                                                     {workspace, workspace_bytes}};
+  for (const auto& in : ins)
+    if (overlap(d_x, nx, in.p, in.n) || overlap(d_w, ndw, in.p, in.n)) return LIZARD_ERR_INVALID_ARG;
+  if (overlap(d_x, nx, d_w, ndw)) return LIZARD_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemsetAsync(workspace, 0, lz::kWsHeader, s) != cudaSuccess) return LIZARD_ERR_CUDA;
+  int launches = 0;
+  const cudaError_t e = lz::launch_fmap_bwd(
+      d.B, d.H, d.L, d.D, d.F, d.dtype, x, w, d_phi, d_x, d_w,
+      static_cast<unsigned char*>(workspace) + lz::kWsHeader, static_cast<unsigned*>(workspace),
+      s, &launches);
+  g_last_launches = launches;
+  return cuda_status(e);
+}
+
 size_t lizard_fwd_bwd_host_workspace_bytes(const lizard_dims* dims, int32_t W) {
   if (!dims_ok(dims) || W < 1 || shape_supported(dims->dk, dims->dv) != LIZARD_OK) return 0;
   const int Hs = host_slice_heads(dims->H);

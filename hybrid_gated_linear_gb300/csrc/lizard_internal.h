@@ -182,6 +182,17 @@ size_t bwd_simt_workspace(int B, int H, int L, int dk, int dv, int M);
 cudaError_t launch_bwd_simt(const BwdArgs& a, lizard_dtype dt, cudaStream_t s, int* launches);
 cudaError_t launch_decode(const DecArgs& a, lizard_dtype dt, cudaStream_t s, int* launches);
 // Segment-state combine and the prefill -> decode ring fill (k_state.cu).
+// Hedgehog feature map (k_fmap.cu).
+bool fmap_tc_supported(int D, int F, lizard_dtype dt);
+bool fmap_simt_supported(int D, int F);
+size_t fmap_bwd_workspace(int B, int H, int L, int D, int F, lizard_dtype dt);
+cudaError_t launch_fmap_fwd(int B, int H, int L, int D, int F, lizard_dtype dt, const void* x,
+                            const void* w, void* phi, unsigned* status, cudaStream_t s,
+                            int* launches);
+cudaError_t launch_fmap_bwd(int B, int H, int L, int D, int F, lizard_dtype dt, const void* x,
+                            const void* w, const void* dphi, void* dx, float* dw,
+                            unsigned char* ws, unsigned* status, cudaStream_t s, int* launches);
+
 cudaError_t launch_state_combine(int units, int dk, int dv, const float* ga, const float* ha,
                                  const float* gb, const float* hb, float* go, float* ho,
                                  cudaStream_t s, int* launches);

@@ -230,6 +230,39 @@ lizard_status lizard_state_combine(int32_t units, int32_t dk, int32_t dv, const 
                                    float* gamma_out, float* h_out, void* stream);
 
 /*
+ * Hedgehog feature map of one projection and its backward ("Lizard", arXiv 2507.09025,
+ * Method: the strictly non-negative map phi(x) = [exp(x W) (+) exp(-x W)] whose
+ * exponential form admits the log-space reparameterisation).  Per (b, h, token):
+ *   z = x W[h]  (F values),   phi = [exp(z_0..z_{F-1}), exp(-z_0..-z_{F-1})]  (2F values).
+ * x [B,H,L,D] T, W [H,D,F] T (one matrix per head, row-major: W[h][d][f]),
+ * phi [B,H,L,2F] T.  The outputs phi are what lizard_attn_fwd takes as phi_q / phi_k
+ * (2F = dk).  D in 1..256, F in 1..128, D*F <= 16384; bf16 with D = 128, F = 64 runs on
+ * tensor cores (fp32 accumulation, bf16 phi), everything else on CUDA cores in fp32.
+ * L = 0 is a no-op (the backward then zero-fills d_w).
+ * Backward, with dphi+ / dphi- the first / last F features of d_phi [B,H,L,2F] T:
+ *   dz = dphi+ exp(z) - dphi- exp(-z),  d_x = dz W^T  [B,H,L,D] T,
+ *   d_w[h] = sum over b and tokens of x^T dz  [H,D,F] fp32, summed in a fixed order
+ *   (run-to-run identical).
+ * Workspace: lizard_feature_map_workspace_bytes (is_bwd 0 or 1); its first word is the
+ * device status word read by lizard_check_device_errors.  Outputs must not overlap
+ * inputs or the workspace.
+ */
+typedef struct lizard_fmap_dims {
+    int32_t B, H, L;      /* batch, heads, tokens (L >= 0) */
+    int32_t D;            /* input features per head */
+    int32_t F;            /* columns of W; phi has 2F features */
+    lizard_dtype dtype;   /* element type of x, W, phi, d_phi, d_x */
+} lizard_fmap_dims;
+
+size_t lizard_feature_map_workspace_bytes(const lizard_fmap_dims* dims, int32_t is_bwd);
+lizard_status lizard_feature_map_fwd(const lizard_fmap_dims* dims, const void* x, const void* w,
+                                     void* phi, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+lizard_status lizard_feature_map_bwd(const lizard_fmap_dims* dims, const void* x, const void* w,
+                                     const void* d_phi, void* d_x, float* d_w, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/*
  * Chunk-local inclusive cumulative sum of log gamma (the reference point of the
  * log-space reparameterisation; "Lizard", arXiv 2507.09025, Method: cumulative gate
  * products c_t).  log_gamma [units,L,dk] fp32 -> b [units,L,dk] fp32 with

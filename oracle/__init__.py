@@ -188,3 +188,26 @@ def state_combine(gamma_a, h_a, gamma_b, h_b):
     [..., dk] and [..., dk, dv]."""
     ga, ha, gb, hb = (_f64(a) for a in (gamma_a, h_a, gamma_b, h_b))
     return ga + gb, np.exp(gb)[..., :, None] * ha + hb
+
+
+def feature_map(x, w):
+    """Hedgehog feature map ("Lizard", arXiv 2507.09025, Method: the strictly
+    non-negative map phi(x) = [exp(x W) (+) exp(-x W)]): x [B,H,L,D], per-head W [H,D,F]
+    -> phi [B,H,L,2F], the F features exp(z) followed by the F features exp(-z) with
+    z = x W.  fp64 numpy."""
+    xx, ww = _f64(x), _f64(w)
+    z = np.einsum("bhld,hdf->bhlf", xx, ww)
+    return np.concatenate([np.exp(z), np.exp(-z)], axis=-1)
+
+
+def feature_map_bwd(x, w, d_phi):
+    """Adjoint of :func:`feature_map`: with z = x W and the two halves dphi+ (first F
+    features) and dphi- (last F) of d_phi, dz = dphi+ exp(z) - dphi- exp(-z),
+    dx = dz W^T and dW[h] = sum over batch and tokens of x^T dz.  Returns (dx, dW)."""
+    xx, ww, dp = _f64(x), _f64(w), _f64(d_phi)
+    F = ww.shape[-1]
+    z = np.einsum("bhld,hdf->bhlf", xx, ww)
+    dz = dp[..., :F] * np.exp(z) - dp[..., F:] * np.exp(-z)
+    dx = np.einsum("bhlf,hdf->bhld", dz, ww)
+    dw = np.einsum("bhld,bhlf->hdf", xx, dz)
+    return dx, dw

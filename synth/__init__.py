@@ -104,6 +104,19 @@ def make_fwd_inputs(B, H, L, dk, dv, M, dtype="bf16", gate="plain", seed=0, with
     return out
 
 
+def make_fmap_inputs(B, H, L, D, F, dtype="bf16", seed=0, with_dphi=False):
+    """Inputs of a feature-map call: x [B,H,L,D] ~ N(0,1) and per-head W [H,D,F] ~
+    N(0, 1/D) (so that x W is about unit variance), each rounded to the storage dtype;
+    with_dphi adds an upstream gradient [B,H,L,2F] ~ N(0,1)."""
+    rng = np.random.default_rng(seed)
+    x = to_storage(rng.standard_normal((B, H, L, D)), dtype)
+    w = to_storage(rng.standard_normal((H, D, F)) / np.sqrt(D), dtype)
+    out = dict(x=x, w=w)
+    if with_dphi:
+        out["d_phi"] = to_storage(rng.standard_normal((B, H, L, 2 * F)), dtype)
+    return out
+
+
 def workload_inputs(name: str, **overrides):
     """Inputs of a named forward/backward workload, optionally with overridden sizes."""
     w = dict(WORKLOADS[name])

@@ -164,3 +164,34 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(lz, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         lz.library()
+
+
+def test_feature_map_rejects_bad_arguments(lib):
+    P = lambda i: ctypes.c_void_p(A + i * 0x1000000)
+    d = lz.lizard_fmap_dims(1, 2, 300, 128, 64, lz.LIZARD_BF16)
+    ws_f = lz.lizard_feature_map_workspace_bytes(d, False)
+    ws_b = lz.lizard_feature_map_workspace_bytes(d, True)
+    assert ws_f == 256
+    # dW partials: one 128x64 fp32 block per (b, h, group of four 128-token tiles)
+    assert ws_b == 256 + 2 * 1 * 128 * 64 * 4
+    fwd = lambda dims=d, x=P(0), w=P(1), phi=P(2), ws=P(3), n=ws_f: lib.lizard_feature_map_fwd(
+        ctypes.byref(dims), x, w, phi, ws, n, None)
+    assert fwd(x=None) == INVALID
+    assert fwd(w=ctypes.c_void_p(A + 8)) == INVALID          # misaligned
+    assert fwd(phi=P(0)) == INVALID                          # output over the input
+    assert fwd(n=ws_f - 1) == WORKSPACE
+    assert fwd(ws=None) == WORKSPACE
+    for bad in (lz.lizard_fmap_dims(1, 2, 300, 0, 64, 1), lz.lizard_fmap_dims(1, 2, 300, 128, 129, 1),
+                lz.lizard_fmap_dims(1, 2, 300, 256, 128, 1), lz.lizard_fmap_dims(0, 2, 300, 128, 64, 1),
+                lz.lizard_fmap_dims(1, 2, -1, 128, 64, 1), lz.lizard_fmap_dims(1, 2, 300, 128, 64, 7)):
+        assert fwd(dims=bad) == INVALID
+        assert lz.lizard_feature_map_workspace_bytes(bad, True) == 0
+    bwd = lambda x=P(0), w=P(1), dp=P(2), dx=P(3), dw=P(4), ws=P(5), n=ws_b: lib.lizard_feature_map_bwd(
+        ctypes.byref(d), x, w, dp, dx, dw, ws, n, None)
+    assert bwd(dw=None) == INVALID
+    assert bwd(dx=P(2)) == INVALID
+    assert bwd(dw=P(3)) == INVALID
+    assert bwd(n=ws_b - 256) == WORKSPACE
+    # both paths keep one partial per 512 tokens, whichever one runs
+    d32 = lz.lizard_fmap_dims(1, 2, 1100, 64, 32, lz.LIZARD_F32)
+    assert lz.lizard_feature_map_workspace_bytes(d32, True) == 256 + 2 * 3 * 64 * 32 * 4

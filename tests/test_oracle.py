@@ -385,3 +385,77 @@ def test_state_combine_of_segments_gives_the_full_state_and_is_associative():
     part = {n: (x[n][:, :, 19:30] if x[n].ndim == 4 else x[n]) for n in _FD_NAMES}
     y = oracle.fwd(*(part[n] for n in _FD_NAMES), W=3, alpha=0.0, h0=h01)["y"]
     np.testing.assert_allclose(y, full["y"][:, :, 19:30], rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------------------------------
+# Hedgehog feature map ("Lizard", arXiv 2507.09025, Method: phi(x) = [exp(xW) (+) exp(-xW)])
+# --------------------------------------------------------------------------------------
+def _fmap_small(B=2, H=2, L=5, D=6, F=4, seed=90):
+    x = synth.make_fmap_inputs(B, H, L, D, F, "f32", seed, with_dphi=True)
+    return {n: a.astype(np.float64) for n, a in x.items()}
+
+
+def test_feature_map_kernel_is_a_sum_of_cosh():
+    """phi(x) . phi(y) = sum_j [e^{a_j} e^{b_j} + e^{-a_j} e^{-b_j}] = 2 sum_j cosh(a_j + b_j)
+    with a = x W, b = y W; the right side is evaluated from (x + y) W with plain loops."""
+    x = _fmap_small()
+    X, Wt = x["x"], x["w"]
+    phi = oracle.feature_map(X, Wt)
+    B, H, L, D = X.shape
+    F = Wt.shape[-1]
+    for b in range(B):
+        for h in range(H):
+            for i in range(L):
+                for j in range(L):
+                    s = 0.0
+                    for f in range(F):
+                        u = sum((X[b, h, i, d] + X[b, h, j, d]) * Wt[h, d, f] for d in range(D))
+                        s += 2.0 * np.cosh(u)
+                    assert abs(float(phi[b, h, i] @ phi[b, h, j]) - s) <= 1e-12 * abs(s)
+
+
+def test_feature_map_special_values_and_symmetry():
+    """phi(0) is all ones; phi is positive; phi(-x) swaps the two halves; the first half
+    of phi(x) for a one-hot x = e_d is exp of row d of W."""
+    x = _fmap_small(seed=91)
+    X, Wt = x["x"], x["w"]
+    F = Wt.shape[-1]
+    np.testing.assert_array_equal(oracle.feature_map(np.zeros_like(X), Wt), 1.0)
+    phi = oracle.feature_map(X, Wt)
+    assert (phi > 0).all()
+    neg = oracle.feature_map(-X, Wt)
+    np.testing.assert_allclose(neg[..., :F], phi[..., F:], rtol=1e-14)
+    np.testing.assert_allclose(neg[..., F:], phi[..., :F], rtol=1e-14)
+    D = X.shape[-1]
+    one = np.zeros((1, Wt.shape[0], D, D))
+    for d in range(D):
+        one[0, :, d, d] = 1.0
+    p1 = oracle.feature_map(one, Wt)
+    for h in range(Wt.shape[0]):
+        for d in range(D):
+            for f in range(F):
+                assert p1[0, h, d, f] == pytest.approx(np.exp(Wt[h, d, f]), rel=1e-15)
+
+
+def test_feature_map_gradients_match_finite_differences():
+    """loss = sum(phi(x; W) * G): central differences in every entry of x and W against
+    feature_map_bwd(x, W, G)."""
+    x = _fmap_small(B=1, H=2, L=3, D=4, F=3, seed=92)
+    X, Wt, G = x["x"], x["w"], x["d_phi"]
+    dx, dw = oracle.feature_map_bwd(X, Wt, G)
+
+    def loss(Xa, Wa):
+        return float((oracle.feature_map(Xa, Wa) * G).sum())
+
+    eps = 1e-6
+    for arr, grad, is_x in ((X, dx, True), (Wt, dw, False)):
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            p, m = arr.copy(), arr.copy()
+            p[idx] += eps
+            m[idx] -= eps
+            lp = loss(p, Wt) if is_x else loss(X, p)
+            lm = loss(m, Wt) if is_x else loss(X, m)
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (is_x, idx, fd, grad[idx])
