@@ -559,8 +559,10 @@ cudaError_t launch_typed(const BwdArgs& a, cudaStream_t s, int* launches) {
   const int BH = a.B * a.H;
   cudaError_t e;
   if (tc && bwd_win_tc_supported(D, D, a.L, a.W, a.M, kDt)) {
-    // The query half of the window backward does not depend on the GLA branch: it runs on
-    // a second stream beside the GLA kernels, and the key half waits for both.
+    // The query half of the window backward and the meta-gradient sum do not depend on the
+    // GLA branch: they run on a second stream beside the GLA kernels.  The key half waits
+    // for the GLA branch and the query half; the caller's stream waits for the meta sum
+    // at the end.
     std::lock_guard<std::mutex> lock(side_stream_lock());
     SideStream* ss = side_stream();
     if (!ss) return cudaErrorNotReady;
@@ -569,9 +571,13 @@ cudaError_t launch_typed(const BwdArgs& a, cudaStream_t s, int* launches) {
     if ((e = launch_bwd_win_q_tc(a, w.dvacc, w.lse, w.Dw, w.mpart, ss->stream, launches)) != cudaSuccess)
       return e;
     if ((e = cudaEventRecord(ss->join, ss->stream)) != cudaSuccess) return e;
+    if ((e = launch_bwd_win_meta_tc(a, w.mpart, ss->stream, launches)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(ss->done, ss->stream)) != cudaSuccess) return e;
     if ((e = launch_bwd_gla_tc(a, w.dvacc, w.gla_tc, s, launches)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(s, ss->join, 0)) != cudaSuccess) return e;
-    return launch_bwd_win_k_tc(a, w.dvacc, w.lse, w.Dw, w.mpart, s, launches);
+    if ((e = launch_bwd_win_k_tc(a, w.dvacc, w.lse, w.Dw, w.mpart, s, launches)) != cudaSuccess)
+      return e;
+    return cudaStreamWaitEvent(s, ss->done, 0);
   }
   if (tc) {
     if ((e = launch_bwd_gla_tc(a, w.dvacc, w.gla_tc, s, launches)) != cudaSuccess) return e;
@@ -588,6 +594,7 @@ cudaError_t launch_typed(const BwdArgs& a, cudaStream_t s, int* launches) {
   }
   if (bwd_win_tc_supported(D, D, a.L, a.W, a.M, kDt)) {
     if ((e = launch_bwd_win_q_tc(a, w.dvacc, w.lse, w.Dw, w.mpart, s, launches)) != cudaSuccess) return e;
+    if ((e = launch_bwd_win_meta_tc(a, w.mpart, s, launches)) != cudaSuccess) return e;
     return launch_bwd_win_k_tc(a, w.dvacc, w.lse, w.Dw, w.mpart, s, launches);
   }
   if (a.L > 0) {

@@ -50,7 +50,9 @@ enum { FF_LD = 0, FF_Z, FF_DONE, FF_COUNT };
 constexpr uint32_t FS_X = 0, FS_W = 32768, FS_BARS = FS_W + 16384;
 constexpr size_t kFwdSmem = FS_BARS + 1024 + 1024;
 
-__global__ void __launch_bounds__(kThreads, 1) fmap_fwd_kernel(const __grid_constant__ FmMaps maps,
+// three CTAs per SM (registers and shared memory), so that one CTA's loads overlap another's
+// epilogue
+__global__ void __launch_bounds__(kThreads, 3) fmap_fwd_kernel(const __grid_constant__ FmMaps maps,
                                                                const FmParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -481,6 +483,9 @@ cudaError_t launch_fmap_fwd(int B, int H, int L, int D, int F, lizard_dtype dt, 
     const FmParams p{H, nt, 1, nullptr, status};
     cudaError_t e = cudaFuncSetAttribute(fmap_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kFwdSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fmap_fwd_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     trace_begin("fmap_fwd_tc", s);
     e = launch_pdl(fmap_fwd_kernel, dim3(B * H * nt), dim3(kThreads), kFwdSmem, s, m, p);
@@ -526,6 +531,9 @@ cudaError_t launch_fmap_bwd(int B, int H, int L, int D, int F, lizard_dtype dt, 
     const FmParams p{H, nt, groups, part, status};
     cudaError_t e = cudaFuncSetAttribute(fmap_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kBwdSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fmap_bwd_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     trace_begin("fmap_bwd_tc", s);
     e = launch_pdl(fmap_bwd_kernel, dim3(B * H * groups), dim3(kThreads), kBwdSmem, s, m, p);

@@ -580,8 +580,8 @@ size_t bwd_win_tc_meta_floats(int BH, int L, int M) {
   return (size_t)BH * ((L + kB - 1) / kB) * M * 256;
 }
 
-// Both halves build the same maps and parameters; `part` selects the query kernel and the
-// meta reduction (0) or the key kernel (1).
+// Both halves build the same maps and parameters; `part` selects the query kernel (0) or
+// the key kernel (1).
 static cudaError_t launch_win_part(int part, const BwdArgs& a, const float* dvacc, float* lse2,
                                    float* Dw, float* mpart, cudaStream_t s, int* launches) {
   const int BH = a.B * a.H, L = a.L;
@@ -626,23 +626,10 @@ static cudaError_t launch_win_part(int part, const BwdArgs& a, const float* dvac
   p.dk = static_cast<bf16*>(a.dk_);
   p.dv = static_cast<bf16*>(a.dvv);
   p.status = a.status;
-  if (part == 1) {
-    const cudaError_t ek = launch_tc(win_k_kernel, km, p, BH * nq, kKSmem, "win_bwd_k_tc", s);
-    ++*launches;
-    return ek;
-  }
-  cudaError_t e = launch_tc(win_q_kernel, qm, p, BH * nq, kQSmem, "win_bwd_q_tc", s);
+  const int grid = BH * nq;
+  cudaError_t e = part == 1 ? launch_tc(win_k_kernel, km, p, grid, kKSmem, "win_bwd_k_tc", s)
+                            : launch_tc(win_q_kernel, qm, p, grid, kQSmem, "win_bwd_q_tc", s);
   ++*launches;
-  if (e != cudaSuccess) return e;
-  // the meta partials come from the query kernel alone
-  if (a.M > 0) {
-    trace_begin("win_bwd_meta", s);
-    e = launch_pdl(win_meta_kernel, dim3(a.H, a.M), dim3(256), 0, s, a.B, a.H, a.M, nq, a.scale,
-                   a.alpha, static_cast<const float*>(mpart), a.dmk, a.dmv);
-    trace_end(s);
-    ++*launches;
-    if (e == cudaSuccess) e = cudaGetLastError();
-  }
   return e;
 }
 
@@ -654,6 +641,19 @@ cudaError_t launch_bwd_win_q_tc(const BwdArgs& a, const float* dvacc, float* lse
 cudaError_t launch_bwd_win_k_tc(const BwdArgs& a, const float* dvacc, float* lse2, float* Dw,
                                 float* mpart, cudaStream_t s, int* launches) {
   return launch_win_part(1, a, dvacc, lse2, Dw, mpart, s, launches);
+}
+
+cudaError_t launch_bwd_win_meta_tc(const BwdArgs& a, const float* mpart, cudaStream_t s,
+                                   int* launches) {
+  if (a.M == 0) return cudaSuccess;
+  const int nq = (a.L + kB - 1) / kB;
+  trace_begin("win_bwd_meta", s);
+  cudaError_t e = launch_pdl(win_meta_kernel, dim3(a.H, a.M), dim3(256), 0, s, a.B, a.H, a.M, nq,
+                             a.scale, a.alpha, mpart, a.dmk, a.dmv);
+  trace_end(s);
+  ++*launches;
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e;
 }
 
 }  // namespace lz

@@ -163,18 +163,21 @@ bool fwd_ctx_usable(int dk, int dv, int L, int W, int M, lizard_dtype dt);
 // lse2/Dw ([B*H][L] fp32) and mpart (bwd_win_tc_meta_floats) as scratch.
 bool bwd_win_tc_supported(int dk, int dv, int L, int W, int M, lizard_dtype dt);
 size_t bwd_win_tc_meta_floats(int BH, int L, int M);
-// The query half (dq, row statistics, meta gradients) and the key half (dk, dv with the
-// GLA part from dvacc); the key half needs the query half's outputs.
+// The query half (dq, row statistics, meta partials), the ordered sum of the meta partials
+// into d_meta_k / d_meta_v, and the key half (dk, dv with the GLA part from dvacc); the
+// meta sum and the key half need the query half's outputs.
 cudaError_t launch_bwd_win_q_tc(const BwdArgs& a, const float* dvacc, float* lse2, float* Dw,
                                 float* mpart, cudaStream_t s, int* launches);
 cudaError_t launch_bwd_win_k_tc(const BwdArgs& a, const float* dvacc, float* lse2, float* Dw,
                                 float* mpart, cudaStream_t s, int* launches);
+cudaError_t launch_bwd_win_meta_tc(const BwdArgs& a, const float* mpart, cudaStream_t s,
+                                   int* launches);
 
 // A second stream of the current device with a fork and a join event, for work that may
 // run beside the caller's stream inside one call; enqueue under side_stream_lock().
 struct SideStream {
   cudaStream_t stream;
-  cudaEvent_t fork, join;
+  cudaEvent_t fork, join, done;
 };
 SideStream* side_stream();
 std::mutex& side_stream_lock();
