@@ -72,10 +72,11 @@ PROFILED_TRAFFIC = {
                     "sha256": "de1faff4a8637d3c238ae54323079a468051cda31f42a494dde9241a1291ab2d"},
     "bwd_suffix": {"bytes_per_token_head": 549, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
                   "sha256": "de1faff4a8637d3c238ae54323079a468051cda31f42a494dde9241a1291ab2d"},
-    "win_bwd_q_tc": {"bytes_per_token_head": 1170, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
-                    "sha256": "80c6456f17c1350e3ef5883ed8e5fc564e6d76f68ce0bb2df629ecff03317e47"},
-    "win_bwd_k_tc": {"bytes_per_token_head": 1876, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
-                    "sha256": "80c6456f17c1350e3ef5883ed8e5fc564e6d76f68ce0bb2df629ecff03317e47"},
+    # window rows re-captured (kernel code as now; only the launch code changed since)
+    "win_bwd_q_tc": {"bytes_per_token_head": 1172, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
+                    "sha256": "151e07ea2f3bcefb27a7db74a71e2a1498cb372c2c334b0371405841cfa39806"},
+    "win_bwd_k_tc": {"bytes_per_token_head": 1874, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
+                    "sha256": "151e07ea2f3bcefb27a7db74a71e2a1498cb372c2c334b0371405841cfa39806"},
 }
 
 DECODE_BYTES_PER_UNIT = 2 * 65536 + 2 * 64 * 128 * 2 + 5 * 256 + 512 + 2 * 256 + 256
