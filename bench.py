@@ -54,6 +54,7 @@ ALGO_BYTES_PER_TOKEN_HEAD = {
     "win_bwd_key": 4 * 256 + 2 * 256,
     "fmap_fwd_tc": 2 * 256,                   # x -> phi (feature map, D = 128, 2F = 128)
     "fmap_bwd_tc": 3 * 256,                   # x, d_phi -> d_x
+    "fwd_prep_fmap": 2 * 256 + 512 + 3 * 256,  # x_q, x_k, log_gamma -> Qt, Kt, e^b
 }
 # DRAM bytes (read + write) per (token, head) from the ncu captures summarised under
 # profiles/, each with the sha256 of the kernel source it was taken on: a kernel whose
@@ -441,7 +442,7 @@ def _decode_part(dev, stream, peaks, steps=64):
                          "algorithmic_bytes_per_step": DECODE_BYTES_PER_UNIT * units}}
 
 
-def _fmap_part(dev, peaks, flush, reps=20):
+def _fmap_part(dev, peaks, flush, prob, reps=20):
     """Hedgehog feature map on the attention workload's shape (B=1, H=32, L=4096, D=128
     input features, F=64, bf16): forward and backward timed separately with CUDA events,
     L2 flushed before each launch.  Algorithmic bytes per (token, head): forward reads x
@@ -462,11 +463,30 @@ def _fmap_part(dev, peaks, flush, reps=20):
     dw = torch.empty(H, D, F, dtype=torch.float32, device=dev)
     fwd = lambda: lz.lizard_feature_map_fwd(dims, X, Wt, phi, ws)
     bwd = lambda: lz.lizard_feature_map_bwd(dims, X, Wt, dp, dx, dw, ws)
+    # the attention forward started from raw projections: fused (exp(+-xW + b) in the prep
+    # pass) against the map applied to x_q and x_k followed by the forward over phi
+    xk_ = synth.make_fmap_inputs(B, H, L, D, F, "bf16", seed=1006)
+    Xk = torch.from_numpy(xk_["x"]).to(dev).to(bf)
+    Wq = (Wt.float() * 0.5).to(bf)
+    Wk = (torch.from_numpy(xk_["w"]).to(dev) * 0.5).to(bf)
+    t, aw = prob.t, prob.w["W"]
+    phik = torch.empty_like(phi)
+    fused = lambda: lz.lizard_attn_fwd_fmap(prob.dims, X, Xk, Wq, Wk, t["v"], t["log_gamma"],
+                                            t["q"], t["k"], t["meta_k"], t["meta_v"], aw, 1.0,
+                                            prob.y, None, None, prob.ws_f)
+
+    def composed():
+        lz.lizard_feature_map_fwd(dims, X, Wq, phi, ws)
+        lz.lizard_feature_map_fwd(dims, Xk, Wk, phik, ws)
+        lz.lizard_attn_fwd(prob.dims, phi, phik, t["v"], t["log_gamma"], t["q"], t["k"],
+                           t["meta_k"], t["meta_v"], aw, 1.0, prob.y, None, None, prob.ws_f)
     out = {"workload": f"Hedgehog feature map B={B}, H={H}, L={L}, D={D}, F={F}, bf16 "
                        "(tensor-core path); L2 flushed before each launch"}
     units = B * H * L
     for name, fn, per_unit, extra in (("fwd", fwd, 2 * 256, H * D * F * 2),
-                                      ("bwd", bwd, 3 * 256, H * D * F * (2 + 4))):
+                                      ("bwd", bwd, 3 * 256, H * D * F * (2 + 4)),
+                                      ("attn_fwd_fused", fused, 2048, 2 * H * D * F * 2),
+                                      ("attn_fwd_composed", composed, 2048, 2 * H * D * F * 2)):
         for _ in range(3):
             fn()
         times = []
@@ -485,8 +505,12 @@ def _fmap_part(dev, peaks, flush, reps=20):
         out[name] = {"us": ms * 1e3, "algorithmic_bytes": nbytes,
                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
                                   "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}}
-    if lz.lizard_check_device_errors(ws) != 0:
+    if lz.lizard_check_device_errors(ws) != 0 or lz.lizard_check_device_errors(prob.ws_f) != 0:
         raise RuntimeError("feature map: device status word set")
+    out["attn_fwd_note"] = ("attention forward from x_q, x_k [B,H,L,128] and W_q, W_k: fused "
+                            "= lizard_attn_fwd_fmap; composed = lizard_feature_map_fwd twice, "
+                            "then lizard_attn_fwd; roofline against the operator's 2048 B per "
+                            "(token, head) with x in place of phi")
     return out
 
 
@@ -630,7 +654,7 @@ def run_ours(args):
     except Exception as e:  # reported, never hidden
         parts["decode"] = {"error": repr(e)}
     try:
-        parts["feature_map"] = _fmap_part(dev, peaks, flush)
+        parts["feature_map"] = _fmap_part(dev, peaks, flush, prob)
     except Exception as e:  # reported, never hidden
         parts["feature_map"] = {"error": repr(e)}
     e2e_ms, h2d, d2h = _e2e(prob, max(3, args.steps // 2), dev)

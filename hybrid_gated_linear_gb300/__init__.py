@@ -26,7 +26,7 @@ __all__ = [
     "lizard_attn_fwd_bwd_host", "lizard_fwd_bwd_host_workspace_bytes",
     "lizard_decode_ring_fill", "lizard_state_combine", "lizard_fmap_dims",
     "lizard_feature_map_fwd", "lizard_feature_map_bwd", "lizard_feature_map_workspace_bytes",
-    "LIZARD_F32", "LIZARD_BF16", "EXPORTED_SYMBOLS",
+    "lizard_attn_fwd_fmap", "LIZARD_F32", "LIZARD_BF16", "EXPORTED_SYMBOLS",
 ]
 
 LIZARD_F32 = 0
@@ -40,7 +40,7 @@ EXPORTED_SYMBOLS = (
     "lizard_abi_version", "lizard_last_launch_count", "lizard_trace_enable", "lizard_trace_read",
     "lizard_decode_step_noalloc", "lizard_attn_fwd_bwd_host", "lizard_fwd_bwd_host_workspace_bytes",
     "lizard_decode_ring_fill", "lizard_state_combine", "lizard_feature_map_fwd",
-    "lizard_feature_map_bwd", "lizard_feature_map_workspace_bytes",
+    "lizard_feature_map_bwd", "lizard_feature_map_workspace_bytes", "lizard_attn_fwd_fmap",
 )
 
 STATUS_NAMES = {0: "LIZARD_OK", 1: "LIZARD_ERR_INVALID_ARG", 2: "LIZARD_ERR_UNSUPPORTED",
@@ -113,6 +113,7 @@ def library():
                 "lizard_decode_ring_fill": (I32, [DDP, I32, I32] + [P] * 5 + [P]),
                 "lizard_state_combine": (I32, [I32, I32, I32] + [P] * 6 + [P]),
                 "lizard_feature_map_workspace_bytes": (SZ, [FMP, I32]),
+                "lizard_attn_fwd_fmap": (I32, [DP] + [P] * 10 + [I32, F, P, P, P, P, SZ, P]),
                 "lizard_feature_map_fwd": (I32, [FMP, P, P, P, P, SZ, P]),
                 "lizard_feature_map_bwd": (I32, [FMP, P, P, P, P, P, P, SZ, P]),
                 "lizard_attn_fwd_bwd_host": (I32, [DP] + [P] * 8 + [I32, F] + [P] * 13 + [P, SZ, P]),
@@ -331,3 +332,14 @@ def lizard_feature_map_bwd(dims: lizard_fmap_dims, x, w, d_phi, d_x, d_w, worksp
                                           _ptr(d_x), _ptr(d_w), _ptr(workspace), _ws_bytes(workspace),
                                           _stream(stream))
     _check(st, "lizard_feature_map_bwd")
+
+
+def lizard_attn_fwd_fmap(dims: lizard_dims, x_q, x_k, w_q, w_k, v, log_gamma, q, k, meta_k,
+                         meta_v, W: int, alpha: float, y, h0, h_final, workspace, stream=None):
+    """Forward pass from the raw projections with the Hedgehog feature map fused into the
+    log-space gate absorption (phi is never formed)."""
+    st = library().lizard_attn_fwd_fmap(
+        ctypes.byref(dims), _ptr(x_q), _ptr(x_k), _ptr(w_q), _ptr(w_k), _ptr(v), _ptr(log_gamma),
+        _ptr(q), _ptr(k), _ptr(meta_k), _ptr(meta_v), int(W), float(alpha), _ptr(y), _ptr(h0),
+        _ptr(h_final), _ptr(workspace), _ws_bytes(workspace), _stream(stream))
+    _check(st, "lizard_attn_fwd_fmap")

@@ -434,7 +434,9 @@ cudaError_t launch_fwd_chunk_tc(const FwdArgs& a, unsigned char* ws, cudaStream_
   cudaError_t e;
   GlaStatesArgs ga{BH, L, a.pq, a.pk, a.lg, a.v, nullptr, a.h0, a.hf, nullptr,
                    w.qt, w.kt, w.eb, w.gam, w.hs, nullptr, a.status};
-  if ((e = launch_gla_prep(ga, s, launches)) != cudaSuccess) return e;
+  e = a.xq ? launch_gla_prep_fmap(ga, a.H, a.xq, a.xk, a.wq, a.wk, s, launches)
+           : launch_gla_prep(ga, s, launches);
+  if (e != cudaSuccess) return e;
   if ((e = launch_gla_scan(ga, GlaScan::kStates, s, launches)) != cudaSuccess) return e;
 
   const int np = a.W <= 65 ? 1 : 2;

@@ -294,6 +294,60 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* phi_q, const 
   return cuda_status(e);
 }
 
+lizard_status lizard_attn_fwd_fmap(const lizard_dims* dims, const void* x_q, const void* x_k,
+                                   const void* w_q, const void* w_k, const void* v,
+                                   const float* log_gamma, const void* q, const void* k,
+                                   const void* meta_k, const void* meta_v, int32_t W,
+                                   float alpha, void* y, const float* h0, float* h_final,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_launches = 0;
+  if (!dims_ok(dims) || W < 1 || !isfinite(alpha)) return LIZARD_ERR_INVALID_ARG;
+  const lizard_dims& d = *dims;
+  const bool tok = d.L > 0;
+  if (!ptr_ok(x_q, !tok) || !ptr_ok(x_k, !tok) || !ptr_ok(w_q, false) || !ptr_ok(w_k, false) ||
+      !ptr_ok(v, !tok) || !ptr_ok(log_gamma, !tok) || !ptr_ok(q, !tok) || !ptr_ok(k, !tok) ||
+      !ptr_ok(y, !tok))
+    return LIZARD_ERR_INVALID_ARG;
+  if (!ptr_ok(meta_k, d.M == 0) || !ptr_ok(meta_v, d.M == 0)) return LIZARD_ERR_INVALID_ARG;
+  if (!ptr_ok(h0, true) || !ptr_ok(h_final, true)) return LIZARD_ERR_INVALID_ARG;
+  const int W_eff = d.L > 0 && W > d.L ? d.L : W;
+  // the fused prologue exists on the tensor-core path only (bf16, x and phi of width 128);
+  // L = 0 has no tokens and only carries h0 to h_final
+  if (d.dtype != LIZARD_BF16 || d.dk != 128 || d.dv != 128) return LIZARD_ERR_UNSUPPORTED;
+  if (tok && !lz::fwd_chunk_tc_supported(d.dk, d.dv, d.L, W_eff, d.M, d.dtype))
+    return LIZARD_ERR_UNSUPPORTED;
+  const size_t need = lizard_fwd_workspace_bytes(dims, W);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return LIZARD_ERR_WORKSPACE;
+  const size_t nt = (size_t)d.B * d.H * d.L * 128 * 2;
+  const size_t nw = (size_t)d.H * 128 * 64 * 2;
+  const size_t nh = (size_t)d.B * d.H * 128 * 128 * sizeof(float);
+  const size_t nm = (size_t)d.H * d.M * 128 * 2;
+  struct Span { const void* p; size_t n; };
+  const Span ins[] = {{x_q, nt}, {x_k, nt}, {w_q, nw}, {w_k, nw}, {v, nt}, {log_gamma, nt * 2},
+                      {q, nt}, {k, nt}, {meta_k, nm}, {meta_v, nm}, {h0, nh},
+                      {workspace, workspace_bytes}};
+  for (const Span& in : ins)
+    if (overlap(y, nt, in.p, in.n) || overlap(h_final, nh, in.p, in.n)) return LIZARD_ERR_INVALID_ARG;
+  if (overlap(y, nt, h_final, nh)) return LIZARD_ERR_INVALID_ARG;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemsetAsync(workspace, 0, lz::kWsHeader, s) != cudaSuccess) return LIZARD_ERR_CUDA;
+  lz::FwdArgs a{d.B, d.H, d.L, d.dk, d.dv, d.M, W_eff, resolve_scale(d.scale, d.dk), alpha,
+                nullptr, nullptr, v, log_gamma, q, k, meta_k, meta_v, y, h0, h_final,
+                static_cast<unsigned*>(workspace),
+                static_cast<unsigned char*>(workspace) + lz::kWsHeader};
+  a.xq = x_q;
+  a.xk = x_k;
+  a.wq = w_q;
+  a.wk = w_k;
+  int launches = 0;
+  // with no tokens the CUDA-core forward only copies h0 to h_final and reads no phi
+  const cudaError_t e = tok ? lz::launch_fwd_chunk_tc(a, a.ws, s, &launches)
+                            : lz::launch_fwd_simt(a, d.dtype, s, &launches);
+  g_last_launches = launches;
+  return cuda_status(e);
+}
+
 lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* phi_q, const void* phi_k,
                               const void* v, const float* log_gamma, const void* q,
                               const void* k, const void* meta_k, const void* meta_v,
@@ -306,8 +360,13 @@ lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* phi_q, const 
   if (!dims_ok(dims) || W < 1 || !isfinite(alpha)) return LIZARD_ERR_INVALID_ARG;
   const lizard_dims& d = *dims;
   const bool tok = d.L > 0;
-  const void* tok_ptrs[] = {phi_q, phi_k, v, log_gamma, q, k, dy,
-                            d_phi_q, d_phi_k, d_v, d_log_gamma, d_q, d_k};
+  const int W_eff = d.L > 0 && W > d.L ? d.L : W;
+  // phi_q / phi_k may be NULL when the forward's saved context stands in for them: the
+  // tensor-core GLA backward given fwd_workspace reads Qt, Kt and e^b, never phi.
+  const bool ctx = fwd_workspace && lz::bwd_gla_tc_supported(d.dk, d.dv, d.L, d.dtype) &&
+                   lz::fwd_ctx_usable(d.dk, d.dv, d.L, W_eff, d.M, d.dtype);
+  if (!ptr_ok(phi_q, !tok || ctx) || !ptr_ok(phi_k, !tok || ctx)) return LIZARD_ERR_INVALID_ARG;
+  const void* tok_ptrs[] = {v, log_gamma, q, k, dy, d_phi_q, d_phi_k, d_v, d_log_gamma, d_q, d_k};
   for (const void* p : tok_ptrs)
     if (!ptr_ok(p, !tok)) return LIZARD_ERR_INVALID_ARG;
   if (!ptr_ok(meta_k, d.M == 0) || !ptr_ok(meta_v, d.M == 0) ||
@@ -342,7 +401,6 @@ lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* phi_q, const 
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = cudaMemsetAsync(workspace, 0, lz::kWsHeader, s);
   if (e != cudaSuccess) return LIZARD_ERR_CUDA;
-  const int W_eff = d.L > 0 && W > d.L ? d.L : W;
   if (W_eff > kMaxBwdWindow) return LIZARD_ERR_UNSUPPORTED;
   lz::BwdArgs a{d.B, d.H, d.L, d.dk, d.dv, d.M, W_eff, resolve_scale(d.scale, d.dk), alpha,
                 phi_q, phi_k, v, log_gamma, q, k, meta_k, meta_v, h0, dy,

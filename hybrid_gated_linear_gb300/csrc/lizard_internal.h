@@ -35,6 +35,9 @@ struct FwdArgs {
   float* hf;
   unsigned* status;
   unsigned char* ws;  // workspace after the header
+  // Set instead of pq/pk when the forward starts from the raw projections and the
+  // Hedgehog feature map (x [B,H,L,128] bf16, one W [128,64] bf16 per head).
+  const void *xq = nullptr, *xk = nullptr, *wq = nullptr, *wk = nullptr;
 };
 
 struct BwdArgs {
@@ -134,6 +137,11 @@ struct GlaStatesArgs {
   unsigned* status;
 };
 cudaError_t launch_gla_prep(const GlaStatesArgs& a, cudaStream_t s, int* launches);
+// The prep pass fused with the Hedgehog feature map (k_prep_fmap_tc.cu): the same Qt, Kt,
+// e^b and Gamma from x_q, x_k [BH][L][128] and per-head W_q, W_k [H][128][64] (bf16), as
+// exp(+-x W_q + b) and exp(+-x W_k - b); needs a.qt, a.kt, a.eb, a.gam, a.lg.
+cudaError_t launch_gla_prep_fmap(const GlaStatesArgs& a, int H, const void* xq, const void* xk,
+                                 const void* wq, const void* wk, cudaStream_t s, int* launches);
 // Which scans: the chunk-start states h_c, the scaled adjoints Gt_c, or both.
 enum class GlaScan { kStates, kAdjoints, kBoth };
 cudaError_t launch_gla_scan(const GlaStatesArgs& a, GlaScan which, cudaStream_t s, int* launches);

@@ -101,6 +101,32 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* phi_q, const 
                               void* stream);
 
 /*
+ * Forward pass started from the raw projections, with the Hedgehog feature map fused into
+ * the log-space absorption of the gate ("Lizard", arXiv 2507.09025, Method: phi(x) =
+ * [exp(xW) (+) exp(-xW)], the cumulative gate absorbed into the query and key features):
+ * the query and key features of the chunkwise form are computed directly as
+ * exp(+-x_q W_q + b) and exp(+-x_k W_k - b) (b the chunk-local cumulative log gate), so
+ * phi is never written.  The result is lizard_attn_fwd with
+ *   phi_q = [exp(x_q W_q), exp(-x_q W_q)],  phi_k = [exp(x_k W_k), exp(-x_k W_k)]
+ * (the map of lizard_feature_map_fwd) up to rounding.
+ *   x_q, x_k [B,H,L,128] bf16; w_q, w_k [H,128,64] bf16 (W[h][d][f]); every other argument
+ *   as in lizard_attn_fwd.  Only bf16 with dk = dv = 128, W <= 129 and M <= 16 (the
+ *   tensor-core forward); other shapes return LIZARD_ERR_UNSUPPORTED -- call
+ *   lizard_feature_map_fwd and lizard_attn_fwd instead.  The workspace is
+ *   lizard_fwd_workspace_bytes(dims, W); it holds the same saved context as
+ *   lizard_attn_fwd's, so lizard_attn_bwd(..., phi_q = NULL, phi_k = NULL, ...,
+ *   fwd_workspace = this workspace) returns d_phi_q, d_phi_k, from which
+ *   lizard_feature_map_bwd gives the gradients of x_q, x_k, W_q, W_k.  A chunk-local
+ *   log-gate sum beyond +-80 sets LIZARD_ERR_DEVICE_CHECK, as in lizard_attn_fwd.
+ */
+lizard_status lizard_attn_fwd_fmap(const lizard_dims* dims, const void* x_q, const void* x_k,
+                                   const void* w_q, const void* w_k, const void* v,
+                                   const float* log_gamma, const void* q, const void* k,
+                                   const void* meta_k, const void* meta_v, int32_t W,
+                                   float alpha, void* y, const float* h0, float* h_final,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Backward pass of lizard_attn_fwd for the loss sum(y * dy).
  *   Inputs as in lizard_attn_fwd plus dy [B,H,L,dv] T.
  *   Outputs: d_phi_q, d_phi_k, d_q, d_k [B,H,L,dk] T; d_v [B,H,L,dv] T (GLA + window);
@@ -112,6 +138,10 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* phi_q, const 
  *   backward reuses instead of recomputing them; a forward that did not leave them (other
  *   shapes or dtypes) is detected from dims and W and the pointer is then ignored.
  *   Passing a workspace that does not match these conditions gives wrong gradients.
+ *   When that context is used (bf16, dk = dv = 128, a forward on the tensor-core path:
+ *   W <= 129 and M <= 16), phi_q and phi_k are not read and may be NULL -- the case of a
+ *   forward started from lizard_attn_fwd_fmap, which never forms phi.  Otherwise NULL
+ *   phi_q / phi_k with L > 0 is LIZARD_ERR_INVALID_ARG.
  * The pages give no backward formulas; this is the exact adjoint of the forward.  The
  * log-gate gradient uses d log_gamma_t = sum_{t'>=t} (phi_q (.) d_phi_q - phi_k (.) d_phi_k)_{t'}
  * (exact because the gate enters only through its cumulative sums).  Deterministic:

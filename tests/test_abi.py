@@ -195,3 +195,27 @@ def test_feature_map_rejects_bad_arguments(lib):
     # both paths keep one partial per 512 tokens, whichever one runs
     d32 = lz.lizard_fmap_dims(1, 2, 1100, 64, 32, lz.LIZARD_F32)
     assert lz.lizard_feature_map_workspace_bytes(d32, True) == 256 + 2 * 3 * 64 * 32 * 4
+
+
+def test_fused_forward_and_phi_free_backward_validation(lib):
+    P = lambda i: ctypes.c_void_p(A + i * 0x10000000)
+    d = lz.lizard_dims(1, 2, 300, 128, 128, 4, lz.LIZARD_BF16, 0.0)
+    ws = lz.lizard_fwd_workspace_bytes(d, 64)
+
+    def fwd(dims=d, xq=P(0), xk=P(1), wq=P(2), wk=P(3), y=P(10)):
+        return lib.lizard_attn_fwd_fmap(ctypes.byref(dims), xq, xk, wq, wk, P(4), P(5), P(6), P(7),
+                                        P(8), P(9), 64, 1.0, y, None, None, P(11), ws, None)
+    assert fwd(xq=None) == INVALID
+    assert fwd(wk=None) == INVALID
+    assert fwd(wq=ctypes.c_void_p(A + 2 * 0x10000000 + 8)) == INVALID  # misaligned
+    # only the tensor-core shape exists fused: fp32 and d = 64 are unsupported
+    for bad in (lz.lizard_dims(1, 2, 300, 128, 128, 4, lz.LIZARD_F32, 0.0),
+                lz.lizard_dims(1, 2, 300, 64, 64, 4, lz.LIZARD_BF16, 0.0)):
+        assert fwd(dims=bad) == UNSUPPORTED
+    # the backward needs phi unless the forward's saved context stands in for it
+    dh = lambda i: ctypes.c_void_p(A + (20 + i) * 0x10000000)
+    wsb = lz.lizard_bwd_workspace_bytes(d, 64)
+    rc = lib.lizard_attn_bwd(ctypes.byref(d), None, None, P(4), P(5), P(6), P(7), P(8), P(9), 64,
+                             1.0, None, P(12), dh(0), dh(1), dh(2), dh(3), dh(4), dh(5), dh(6),
+                             dh(7), None, None, dh(8), wsb, None)
+    assert rc == INVALID

@@ -117,3 +117,122 @@ def test_feature_map_output_feeds_the_attention_forward():
     assert rel_l2(y, ref) <= TOL["bf16"]
     ref_phi = oracle.feature_map(fq["x"], fq["w"]) / np.sqrt(128)
     assert rel_l2(pq, ref_phi) <= TOL["bf16"]
+
+
+# --------------------------------------------------------------------------------------
+# forward from the raw projections with the feature map fused into the gate absorption
+# --------------------------------------------------------------------------------------
+def _fused_inputs(B, H, L, M, seed):
+    base = synth.make_fwd_inputs(B, H, L, 128, 128, M, "bf16", "plain", seed=seed, with_dy=True)
+    fq = synth.make_fmap_inputs(B, H, L, 128, 64, "bf16", seed=seed + 1)
+    fk = synth.make_fmap_inputs(B, H, L, 128, 64, "bf16", seed=seed + 2)
+    # W ~ N(0, 1/(4D)) keeps phi_q . phi_k moderate
+    x = dict(base, x_q=fq["x"], x_k=fk["x"], w_q=synth.to_storage(fq["w"] * 0.5, "bf16"),
+             w_k=synth.to_storage(fk["w"] * 0.5, "bf16"))
+    x["phi_q"] = oracle.feature_map(x["x_q"], x["w_q"])
+    x["phi_k"] = oracle.feature_map(x["x_k"], x["w_k"])
+    return x
+
+
+def _run_fused(x, W, alpha, h0=None, want_hf=True):
+    import torch
+    import hybrid_gated_linear_gb300 as lz
+    bf = torch.bfloat16
+    B, H, L, _ = x["x_q"].shape
+    M = x["meta_k"].shape[1]
+    t = {n: torch.from_numpy(np.ascontiguousarray(x[n])).cuda() for n in
+         ("x_q", "x_k", "w_q", "w_k", "v", "q", "k", "meta_k", "meta_v", "log_gamma")}
+    for n in t:
+        if n != "log_gamma":
+            t[n] = t[n].to(bf)
+    dims = lz.lizard_dims(B, H, L, 128, 128, M, lz.LIZARD_BF16, 0.0)
+    ws = torch.zeros(lz.lizard_fwd_workspace_bytes(dims, W), dtype=torch.uint8, device="cuda")
+    y = torch.empty(B, H, L, 128, dtype=bf, device="cuda")
+    hf = torch.empty(B, H, 128, 128, dtype=torch.float32, device="cuda") if want_hf else None
+    h0t = None if h0 is None else torch.from_numpy(np.ascontiguousarray(h0, dtype=np.float32)).cuda()
+    lz.lizard_attn_fwd_fmap(dims, t["x_q"], t["x_k"], t["w_q"], t["w_k"], t["v"], t["log_gamma"],
+                            t["q"], t["k"], t["meta_k"], t["meta_v"], W, alpha, y, h0t, hf, ws)
+    return t, dims, ws, y, hf
+
+
+@pytest.mark.parametrize("B,H,L,W,M,alpha,with_h0", [(1, 2, 300, 64, 4, 1.0, False),
+                                                     (2, 2, 129, 100, 0, 0.7, True),
+                                                     (1, 1, 1, 64, 4, 1.0, False),
+                                                     (1, 3, 700, 37, 8, 1.3, True)])
+def test_fused_feature_map_forward_matches_oracle(B, H, L, W, M, alpha, with_h0):
+    import hybrid_gated_linear_gb300 as lz
+    x = _fused_inputs(B, H, L, M, seed=700 + L)
+    h0 = (np.random.default_rng(701).standard_normal((B, H, 128, 128)) * 0.1) if with_h0 else None
+    _, _, ws, y, hf = _run_fused(x, W, alpha, h0=h0)
+    assert lz.lizard_check_device_errors(ws) == 0
+    ref = oracle.fwd(*(x[n] for n in NAMES), W=W, alpha=alpha, h0=h0, want_state=True)
+    errs = {"y": rel_l2(host(y), ref["y"]), "h_final": rel_l2(hf.cpu().numpy(), ref["h_final"])}
+    assert max(errs.values()) <= TOL["bf16"], errs
+
+
+def test_fused_forward_agrees_with_the_map_followed_by_the_forward():
+    import torch
+    import hybrid_gated_linear_gb300 as lz
+    x = _fused_inputs(1, 2, 500, 4, seed=710)
+    t, dims, ws, y, _ = _run_fused(x, 64, 1.0, want_hf=False)
+    fd = lz.lizard_fmap_dims(1, 2, 500, 128, 64, lz.LIZARD_BF16)
+    wsf = torch.zeros(lz.lizard_feature_map_workspace_bytes(fd, False), dtype=torch.uint8, device="cuda")
+    pq = torch.empty(1, 2, 500, 128, dtype=torch.bfloat16, device="cuda")
+    pk = torch.empty_like(pq)
+    lz.lizard_feature_map_fwd(fd, t["x_q"], t["w_q"], pq, wsf)
+    lz.lizard_feature_map_fwd(fd, t["x_k"], t["w_k"], pk, wsf)
+    y2 = torch.empty_like(y)
+    ws2 = torch.zeros_like(ws)
+    lz.lizard_attn_fwd(dims, pq, pk, t["v"], t["log_gamma"], t["q"], t["k"], t["meta_k"],
+                       t["meta_v"], 64, 1.0, y2, None, None, ws2)
+    assert lz.lizard_check_device_errors(ws) == 0 and lz.lizard_check_device_errors(ws2) == 0
+    assert rel_l2(host(y), host(y2)) <= 1e-2
+
+
+@pytest.mark.parametrize("L,W", [(300, 64), (129, 100)])
+def test_fused_training_step_gradients_match_oracle(L, W):
+    """Forward from x, backward with phi = NULL and the forward's workspace, then the
+    feature map's backward: every gradient against the oracle chain (attention adjoint,
+    then the feature map's adjoint)."""
+    import torch
+    import hybrid_gated_linear_gb300 as lz
+    B, H, M = 2, 2, 4
+    x = _fused_inputs(B, H, L, M, seed=720 + L)
+    t, dims, ws, y, _ = _run_fused(x, W, 1.0, want_hf=False)
+    bf = torch.bfloat16
+    dy = torch.from_numpy(x["dy"]).cuda().to(bf)
+    wsb = torch.zeros(lz.lizard_bwd_workspace_bytes(dims, W), dtype=torch.uint8, device="cuda")
+    g = {n: torch.empty(B, H, L, 128, dtype=bf, device="cuda")
+         for n in ("d_phi_q", "d_phi_k", "d_v", "d_q", "d_k")}
+    g["d_log_gamma"] = torch.empty(B, H, L, 128, dtype=torch.float32, device="cuda")
+    g["d_meta_k"] = torch.empty(H, M, 128, dtype=torch.float32, device="cuda")
+    g["d_meta_v"] = torch.empty(H, M, 128, dtype=torch.float32, device="cuda")
+    lz.lizard_attn_bwd(dims, None, None, t["v"], t["log_gamma"], t["q"], t["k"], t["meta_k"],
+                       t["meta_v"], W, 1.0, None, dy, g["d_phi_q"], g["d_phi_k"], g["d_v"],
+                       g["d_log_gamma"], g["d_q"], g["d_k"], g["d_meta_k"], g["d_meta_v"], None,
+                       wsb, fwd_workspace=ws)
+    fd = lz.lizard_fmap_dims(B, H, L, 128, 64, lz.LIZARD_BF16)
+    wsf = torch.zeros(lz.lizard_feature_map_workspace_bytes(fd, True), dtype=torch.uint8, device="cuda")
+    out = {}
+    for s in ("q", "k"):
+        dxs = torch.empty(B, H, L, 128, dtype=bf, device="cuda")
+        dws = torch.empty(H, 128, 64, dtype=torch.float32, device="cuda")
+        lz.lizard_feature_map_bwd(fd, t["x_" + s], t["w_" + s], g["d_phi_" + s], dxs, dws, wsf)
+        out["dx_" + s], out["dw_" + s] = host(dxs), dws.cpu().numpy()
+    for w in (ws, wsb, wsf):
+        assert lz.lizard_check_device_errors(w) == 0
+    ref = oracle.bwd(*(x[n] for n in NAMES), x["dy"], W=W, alpha=1.0)
+    errs = {n: rel_l2(host(gt), ref[n]) for n, gt in g.items()}
+    for s in ("q", "k"):
+        dxr, dwr = oracle.feature_map_bwd(x["x_" + s], x["w_" + s], ref["d_phi_" + s])
+        errs["dx_" + s] = rel_l2(out["dx_" + s], dxr)
+        errs["dw_" + s] = rel_l2(out["dw_" + s], dwr)
+    assert max(errs.values()) <= TOL["bf16"], errs
+
+
+def test_fused_forward_flags_gate_sums_out_of_range():
+    import hybrid_gated_linear_gb300 as lz
+    x = _fused_inputs(1, 1, 256, 4, seed=730)
+    x["log_gamma"] = np.full_like(x["log_gamma"], -2.0)  # chunk sums reach -256
+    _, _, ws, _, _ = _run_fused(x, 64, 1.0, want_hf=False)
+    assert lz.lizard_check_device_errors(ws) == 5  # LIZARD_ERR_DEVICE_CHECK
