@@ -514,6 +514,57 @@ def _fmap_part(dev, peaks, flush, prob, reps=20):
     return out
 
 
+def _long_context_part(dev, peaks, flush, reps=5):
+    """Long-context forward with few (batch, head) units: B=1, H=4, L=65536, W=128, M=8
+    (the 64K shape with 4 heads), where the state scan is split into segments.  Forward
+    timed with CUDA events (L2 flushed before each call), then one traced call for the
+    per-kernel times."""
+    import torch
+
+    import hybrid_gated_linear_gb300 as lz
+    import synth
+    B, H, L, d, W, M = 1, 4, 65536, 128, 128, 8
+    x = synth.make_fwd_inputs(B, H, L, d, d, M, "bf16", "bimodal", seed=1007)
+    bf = torch.bfloat16
+    t = {n: torch.from_numpy(a).to(dev) for n, a in x.items()}
+    for n in t:
+        if n != "log_gamma":
+            t[n] = t[n].to(bf)
+    dims = lz.lizard_dims(B, H, L, d, d, M, lz.LIZARD_BF16, 0.0)
+    ws = torch.zeros(lz.lizard_fwd_workspace_bytes(dims, W), dtype=torch.uint8, device=dev)
+    y = torch.empty(B, H, L, d, dtype=bf, device=dev)
+    fwd = lambda: lz.lizard_attn_fwd(dims, *(t[n] for n in NAMES), W, 1.0, y, None, None, ws)
+    for _ in range(2):
+        fwd()
+    times = []
+    for _ in range(reps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fwd()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    launches = lz.lizard_last_launch_count()
+    lz.lizard_trace_enable(True)
+    flush()
+    fwd()
+    lz.lizard_trace_enable(False)
+    trace = lz.lizard_trace_read()
+    if lz.lizard_check_device_errors(ws) != 0:
+        raise RuntimeError("long-context forward: device status word set")
+    ms = statistics.mean(times)
+    units = B * H * L
+    gbs = 2048 * units / (ms * 1e-3) / 1e9
+    return {"workload": f"long-context forward B={B}, H={H}, L={L}, d={d}, W={W}, M={M}, bf16 "
+                        "(state scan split into segments)",
+            "ms": ms, "tokens_per_s": B * L / (ms * 1e-3), "launches": launches,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": 2048 * units},
+            "kernels_ms": {name: round(v, 4) for name, v in trace}}
+
+
 def _e2e(prob, steps, dev):
     """The same fwd+bwd step through the host-memory entry point lizard_attn_fwd_bwd_host:
     pinned host buffers, every input copied to the device and y plus every gradient
@@ -657,6 +708,10 @@ def run_ours(args):
         parts["feature_map"] = _fmap_part(dev, peaks, flush, prob)
     except Exception as e:  # reported, never hidden
         parts["feature_map"] = {"error": repr(e)}
+    try:
+        parts["long_context"] = _long_context_part(dev, peaks, flush)
+    except Exception as e:  # reported, never hidden
+        parts["long_context"] = {"error": repr(e)}
     e2e_ms, h2d, d2h = _e2e(prob, max(3, args.steps // 2), dev)
     e2e_ms = _max_over_ranks(e2e_ms, world, dev)
 

@@ -42,6 +42,7 @@ struct GlaWs {
   float* gam;          // [BH][nc][128]
   bf16 *hs, *gs;       // [BH][nc][128][128]
   float* rtot;         // [BH][nc][128]
+  float* seg;          // scratch of a split scan, or null
 };
 
 size_t gla_ws_layout(int BH, int L, unsigned char* p, GlaWs* w) {
@@ -63,6 +64,8 @@ size_t gla_ws_layout(int BH, int L, unsigned char* p, GlaWs* w) {
   g.hs = reinterpret_cast<bf16*>(take(st));
   g.gs = reinterpret_cast<bf16*>(take(st));
   g.rtot = reinterpret_cast<float*>(take(vec));
+  const size_t seg = gla_seg_scratch(BH, L);
+  g.seg = seg ? reinterpret_cast<float*>(take(seg)) : nullptr;
   if (w) *w = g;
   return off;
 }
@@ -448,7 +451,7 @@ cudaError_t launch_bwd_gla_tc(const BwdArgs& a, float* dvacc, unsigned char* ws,
     w.hs = fc.hs;
   }
   GlaStatesArgs ga{BH, L, a.pq, a.pk, a.lg, a.v, a.dy, a.h0, nullptr, a.dh0,
-                   w.qt, w.kt, w.eb, w.gam, w.hs, w.gs, a.status};
+                   w.qt, w.kt, w.eb, w.gam, w.hs, w.gs, a.status, w.seg};
   if (!ctx && (e = launch_gla_prep(ga, s, launches)) != cudaSuccess) return e;
   if ((e = launch_gla_scan(ga, ctx ? GlaScan::kAdjoints : GlaScan::kBoth, s, launches)) != cudaSuccess)
     return e;

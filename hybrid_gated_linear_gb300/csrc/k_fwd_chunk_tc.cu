@@ -395,6 +395,8 @@ size_t fwd_ws_layout(int BH, int L, unsigned char* p, FwdWs* w) {
   g.eb = reinterpret_cast<bf16*>(take((size_t)BH * L * kD * sizeof(bf16)));
   g.gam = reinterpret_cast<float*>(take((size_t)BH * nc * kD * sizeof(float)));
   g.hs = reinterpret_cast<bf16*>(take((size_t)BH * nc * kD * kD * sizeof(bf16)));
+  const size_t seg = gla_seg_scratch(BH, L);
+  g.seg = seg ? reinterpret_cast<float*>(take(seg)) : nullptr;
   if (w) *w = g;
   return off;
 }
@@ -433,7 +435,7 @@ cudaError_t launch_fwd_chunk_tc(const FwdArgs& a, unsigned char* ws, cudaStream_
   fwd_ws_layout(BH, L, ws, &w);
   cudaError_t e;
   GlaStatesArgs ga{BH, L, a.pq, a.pk, a.lg, a.v, nullptr, a.h0, a.hf, nullptr,
-                   w.qt, w.kt, w.eb, w.gam, w.hs, nullptr, a.status};
+                   w.qt, w.kt, w.eb, w.gam, w.hs, nullptr, a.status, w.seg};
   e = a.xq ? launch_gla_prep_fmap(ga, a.H, a.xq, a.xk, a.wq, a.wk, s, launches)
            : launch_gla_prep(ga, s, launches);
   if (e != cudaSuccess) return e;

@@ -113,7 +113,7 @@ struct ScanCfg {
 template <int kStages, int SL>
 __global__ void __launch_bounds__(kScanThreads, 1)
 scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc, int ndir,
-            int dir0) {
+            int dir0, int nseg, int cps, float* segf0, float* segf1) {
   using SC = ScanCfg<kStages, SL>;
   enum { S_FULL = SC::S_FULL, S_EMPTY = SC::S_EMPTY, S_DFULL = SC::S_DFULL,
          S_DFREE = SC::S_DFREE, S_DONE = SC::S_DONE, S_COUNT = SC::S_COUNT };
@@ -127,7 +127,11 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int dir = ndir == 2 ? (blockIdx.x & 1) : dir0;
   const int sl = (blockIdx.x / ndir) % kSlicesT;
-  const int bh = blockIdx.x / (ndir * kSlicesT);
+  const int seg = (blockIdx.x / (ndir * kSlicesT)) % nseg;
+  const int bh = blockIdx.x / (ndir * kSlicesT * nseg);
+  // this CTA's chunks [cb, ce): the whole sequence, or one segment of a split sequence
+  // (each segment scanned from zero; the segments are joined afterwards)
+  const int cb = seg * cps, ce = min(nc, cb + cps), nl = ce - cb;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S_COUNT; ++i)
@@ -151,8 +155,8 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
       const CUtensorMap* my = dir ? &maps.y1 : &maps.y0;
       uint32_t armed[kStages] = {};
       bool ok = true;
-      for (int u = 0; u < nc && ok; ++u) {
-        const int c = dir ? nc - 1 - u : u, s = u % kStages, k = u / kStages;
+      for (int u = 0; u < nl && ok; ++u) {
+        const int c = dir ? ce - 1 - u : cb + u, s = u % kStages, k = u / kStages;
         if (k >= 1 && !(ok = wait_bar(ctl, S_EMPTY + s, (k - 1) & 1))) break;
         unsigned char* st = sm + s * kStageB;
         mbar_arrive_expect_tx(&ctl->bar[S_FULL + s], kStageB);
@@ -180,7 +184,7 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
       const uint32_t id = idesc_bf16(kD, SL, true, true);
       const uint32_t sbase = smem_u32(sm);
       bool ok = true;
-      for (int u = 0; u < nc && ok; ++u) {
+      for (int u = 0; u < nl && ok; ++u) {
         const int s = u % kStages, k = u / kStages;
         if (!(ok = wait_bar(ctl, S_FULL + s, k & 1))) break;
         if (k >= 1 && !(ok = wait_bar(ctl, S_DFREE + s, (k - 1) & 1))) break;
@@ -203,7 +207,7 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
     const int i = qw * 32 + lane;  // state row = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(qw * 32) << 16);
     float x[SL];
-    if (dir == 0 && p.h0) {
+    if (dir == 0 && nseg == 1 && p.h0) {  // a split scan joins h0 in afterwards
       const float4* src = reinterpret_cast<const float4*>(p.h0 + ((size_t)bh * kD + i) * kD + sl * SL);
 #pragma unroll
       for (int k = 0; k < SL / 4; ++k) {
@@ -223,14 +227,14 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
     // with independent loads into its own column of shared memory (read back by the same
     // thread only), so a global load's latency is paid once per kGamAhead chunks.
     float* gsm = reinterpret_cast<float*>(sm + SC::kGam);
-    for (int u = 0; u < nc && ok; ++u) {
-      const int c = dir ? nc - 1 - u : u, s = u % kStages;
+    for (int u = 0; u < nl && ok; ++u) {
+      const int c = dir ? ce - 1 - u : cb + u, s = u % kStages;
       if (u % kGamAhead == 0) {
-        const int cnt = min(kGamAhead, nc - u);
+        const int cnt = min(kGamAhead, nl - u);
         float gv[kGamAhead];
 #pragma unroll
         for (int v = 0; v < kGamAhead; ++v) {
-          const int cv = dir ? nc - 1 - (u + v) : u + v;
+          const int cv = dir ? ce - 1 - (u + v) : cb + u + v;
           gv[v] = v < cnt ? p.gam[((size_t)bh * nc + cv) * kD + i] : 0.f;
         }
 #pragma unroll
@@ -267,9 +271,14 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
       mbar_arrive(&ctl->bar[S_DFREE + s]);
     }
     if (!ok) ctl->abort = 1;
-    float* fin = dir ? p.dh0 : p.hf;
+    // the final state (h_final / d h0), or this segment's state from zero for the join
+    float* fin = nullptr;
+    if (nseg > 1)
+      fin = (dir ? segf1 : segf0) + (size_t)(bh * nseg + seg) * kD * kD;
+    else if (float* f = dir ? p.dh0 : p.hf)
+      fin = f + (size_t)bh * kD * kD;
     if (ok && fin) {
-      float4* dst = reinterpret_cast<float4*>(fin + ((size_t)bh * kD + i) * kD + sl * SL);
+      float4* dst = reinterpret_cast<float4*>(fin + (size_t)i * kD + sl * SL);
 #pragma unroll
       for (int k = 0; k < SL / 4; ++k) dst[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
     }
@@ -297,7 +306,8 @@ cudaError_t launch_gla_prep(const GlaStatesArgs& a, cudaStream_t s, int* launche
 }
 
 template <int kStages, int SL>
-cudaError_t scan_variant(const GlaStatesArgs& a, bool states, bool adjoints, int nc, cudaStream_t s) {
+cudaError_t scan_variant(const GlaStatesArgs& a, bool states, bool adjoints, int nc, int nseg,
+                         int cps, float* segf0, float* segf1, cudaStream_t s) {
   using SC = ScanCfg<kStages, SL>;
   const uint64_t bhl = (uint64_t)a.BH, Ll = (uint64_t)a.L;
   const uint32_t ybox = SL == 32 ? 32 : 64;
@@ -321,29 +331,51 @@ cudaError_t scan_variant(const GlaStatesArgs& a, bool states, bool adjoints, int
   }
   const int ndir = states && adjoints ? 2 : 1;
   const int dir0 = states ? 0 : 1;
-  const int grid = a.BH * (kD / SL) * ndir;
+  const int grid = a.BH * (kD / SL) * ndir * nseg;
   auto kern = scan_kernel<kStages, SL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SC::kSmem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(kScanThreads), SC::kSmem, s, m, a, nc, ndir, dir0);
+  return launch_pdl(kern, dim3(grid), dim3(kScanThreads), SC::kSmem, s, m, a, nc, ndir, dir0,
+                    nseg, cps, segf0, segf1);
 }
 
 cudaError_t launch_gla_scan(const GlaStatesArgs& a, GlaScan which, cudaStream_t s, int* launches) {
   const int nc = (a.L + kC - 1) / kC;
   const bool states = which != GlaScan::kAdjoints, adjoints = which != GlaScan::kStates;
   const int ndir = states && adjoints ? 2 : 1;
+  // With few (b, h) units the chunks of each are split into segments scanned in parallel
+  // and joined afterwards (k_scan_seg.cu).
+  const int cap = gla_seg_cap(a.BH, nc);
+  int nseg = a.seg ? gla_scan_segments(a.BH, nc, ndir) : 1;
+  int cps = nc;
+  if (nseg > 1) {
+    cps = (nc + nseg - 1) / nseg;
+    nseg = (nc + cps - 1) / cps;  // no empty segment
+  }
+  float* segf0 = nseg > 1 ? a.seg : nullptr;
+  float* segf1 = nseg > 1 ? a.seg + (size_t)2 * a.BH * cap * kD * kD : nullptr;
   // 32 value columns per CTA: measured against 64 and 128 (which read each Kt/Qt tile fewer
   // times), the narrow slice keeps the per-chunk chain of every CTA shortest.
   trace_begin(adjoints ? "bwd_scan_tc" : "fwd_scan_tc", s);
   // five chunks in flight when the grid fits one wave (measured against four: 27.9 -> 26.7
   // us on B=1, H=32, L=4096), else two so that two CTAs share an SM
-  const cudaError_t e = a.BH * 4 * ndir <= ctas_per_wave(1)
-                            ? scan_variant<5, 32>(a, states, adjoints, nc, s)
-                            : scan_variant<2, 32>(a, states, adjoints, nc, s);
+  cudaError_t e = a.BH * 4 * ndir * nseg <= ctas_per_wave(1)
+                      ? scan_variant<5, 32>(a, states, adjoints, nc, nseg, cps, segf0, segf1, s)
+                      : scan_variant<2, 32>(a, states, adjoints, nc, nseg, cps, segf0, segf1, s);
   trace_end(s);
   ++*launches;
-  return e;
+  if (e != cudaSuccess || nseg == 1) return e;
+  for (int dir = 0; dir < 2; ++dir) {
+    if ((dir == 0 && !states) || (dir == 1 && !adjoints)) continue;
+    e = launch_seg_join(a.BH, nc, nseg, cps, dir, a.gam, a.seg, cap, dir == 0 ? a.h0 : nullptr,
+                        dir == 0 ? a.hf : a.dh0, s, launches);
+    if (e == cudaSuccess)
+      e = launch_seg_fix(a.BH, nc, nseg, cps, dir, a.gam, a.seg, cap, dir == 0 ? a.hs : a.gs,
+                         dir == 0 && a.h0 != nullptr, s, launches);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace lz

@@ -135,6 +135,8 @@ struct GlaStatesArgs {
   float* gam;
   bf16 *hs, *gs;
   unsigned* status;
+  // gla_seg_scratch bytes for a split scan (null: never split)
+  float* seg = nullptr;
 };
 cudaError_t launch_gla_prep(const GlaStatesArgs& a, cudaStream_t s, int* launches);
 // The prep pass fused with the Hedgehog feature map (k_prep_fmap_tc.cu): the same Qt, Kt,
@@ -142,6 +144,19 @@ cudaError_t launch_gla_prep(const GlaStatesArgs& a, cudaStream_t s, int* launche
 // exp(+-x W_q + b) and exp(+-x W_k - b); needs a.qt, a.kt, a.eb, a.gam, a.lg.
 cudaError_t launch_gla_prep_fmap(const GlaStatesArgs& a, int H, const void* xq, const void* xk,
                                  const void* wq, const void* wk, cudaStream_t s, int* launches);
+// Sequence split of the scans (k_scan_seg.cu): when the B*H units leave most SMs idle,
+// each unit's chunks are cut into segments scanned in parallel from zero and then joined.
+constexpr int kSegMinChunks = 8;  // chunks per segment at least
+constexpr int kSegMaxCtas = 256;  // bound on the CTAs of one scan wave, for sizing scratch
+int gla_seg_cap(int BH, int nc);                // segments the scratch is sized for (1: none)
+size_t gla_seg_scratch(int BH, int L);          // bytes, 0 when never split
+int gla_scan_segments(int BH, int nc, int ndir);  // segments to use on this device (1: none)
+cudaError_t launch_seg_join(int BH, int nc, int nseg, int cps, int dir, const float* gam,
+                            float* seg, int cap, const float* h0, float* fin, cudaStream_t s,
+                            int* launches);
+cudaError_t launch_seg_fix(int BH, int nc, int nseg, int cps, int dir, const float* gam,
+                           float* seg, int cap, bf16* st, bool with_h0, cudaStream_t s,
+                           int* launches);
 // Which scans: the chunk-start states h_c, the scaled adjoints Gt_c, or both.
 enum class GlaScan { kStates, kAdjoints, kBoth };
 cudaError_t launch_gla_scan(const GlaStatesArgs& a, GlaScan which, cudaStream_t s, int* launches);
@@ -152,6 +167,7 @@ struct GlaCtx {
   bf16 *qt, *kt, *eb;
   float* gam;
   bf16* hs;
+  float* seg = nullptr;  // scratch of a split scan (not part of the reused context)
 };
 // The context inside a forward workspace (after its header) of B*H units of L tokens.
 GlaCtx fwd_chunk_tc_ctx(int BH, int L, unsigned char* ws);
