@@ -90,12 +90,15 @@ struct ChunkP {
 };
 
 enum {
-  M_LD0 = 0, M_LD1, M_LD2, M_LD3, M_A, M_P, M_AS, M_PS, M_DQK, M_DV, M_EB, M_DONE, M_COUNT
+  M_LD0 = 0, M_LD1, M_LD2, M_LD3, M_A, M_P, M_AS, M_PS, M_DV, M_EB, M_DONE, M_COUNT
 };
 constexpr uint32_t kTile = kC * kD * 2;  // 32 KB
+// seven 32 KB tiles (e^b has its own, so it loads with the others), the [8][32] partial
+// sums of r, the barriers: the 227 KB a CTA may have
 constexpr uint32_t C_DY = 0, C_V = kTile, C_QT = 2 * kTile, C_KT = 3 * kTile, C_HS = 4 * kTile,
-                   C_GS = 5 * kTile, C_RED = 6 * kTile, C_BARS = C_RED + 2048;
+                   C_GS = 5 * kTile, C_EB = 6 * kTile, C_RED = 7 * kTile, C_BARS = C_RED + 1024;
 constexpr size_t kChunkSmem = C_BARS + 1024 + 1024;
+static_assert(kChunkSmem <= 232448, "shared memory per CTA");
 constexpr int kChunkThreads = 10 * 32;
 constexpr int kEpiThreads = 8 * 32;
 // TMEM columns
@@ -148,9 +151,9 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
       tma_load_3d(sm + C_QT + kTile / 2, &maps.qt, 64, t0, bh, &ctl->bar[M_LD3]);
       tma_load_3d(sm + C_KT, &maps.kt, 0, t0, bh, &ctl->bar[M_LD3]);
       tma_load_3d(sm + C_KT + kTile / 2, &maps.kt, 64, t0, bh, &ctl->bar[M_LD3]);
-      // e^b is loaded only once dQt and dKt are done; bring it into L2 now
-      tma_prefetch_l2_3d(&maps.eb, 0, t0, bh);
-      tma_prefetch_l2_3d(&maps.eb, 64, t0, bh);
+      mbar_arrive_expect_tx(&ctl->bar[M_EB], kTile);
+      tma_load_3d(sm + C_EB, &maps.eb, 0, t0, bh, &ctl->bar[M_EB]);
+      tma_load_3d(sm + C_EB + kTile / 2, &maps.eb, 64, t0, bh, &ctl->bar[M_EB]);
       // Once this tile's inputs are in, warm L2 with those of the tile one wave later, so
       // that its loads overlap this tile's tensor-core and epilogue phases.
       const int nb = blockIdx.x + p.ahead;
@@ -166,17 +169,9 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
           tma_prefetch_l2_3d(&maps.eb, x, nt0, nbh);
         }
       }
-      // e^b goes over the masked A tile once dQt and dKt are complete
-      uint32_t armed_eb = 0;
-      if (wait_bar(ctl, M_DQK, 0)) {
-        mbar_arrive_expect_tx(&ctl->bar[M_EB], kTile);
-        tma_load_3d(sm + C_HS, &maps.eb, 0, t0, bh, &ctl->bar[M_EB]);
-        tma_load_3d(sm + C_HS + kTile / 2, &maps.eb, 64, t0, bh, &ctl->bar[M_EB]);
-        armed_eb = 1;
-      }
       const uint64_t tw = globaltimer_ns();
       for (int b = M_LD0; b <= M_LD3; ++b) drain_bar(ctl, b, 1, tw);
-      drain_bar(ctl, M_EB, armed_eb, tw);
+      drain_bar(ctl, M_EB, 1, tw);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -216,7 +211,6 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
         tc_fence_after();
         mma_kn(T_DQ, sb + C_HS, sb + C_KT, true);   // dQt += A Kt
         mma_nn(T_DK, sb + C_HS, sb + C_QT, true);   // dKt += A^T Qt
-        mma_commit(&ctl->bar[M_DQK]);
         mma_kn(T_A, sb + C_KT, sb + C_GS, false);   // dV   = Kt Gt
       }
       if (ok && (ok = wait_bar(ctl, M_PS, 0))) {
@@ -279,8 +273,8 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
     // d phi_q, d phi_k, the log-gate term r summed from the chunk's end, and the GLA part
     // of dv, in four rounds of 32 columns (16 per thread).  Each round is staged in one of
     // two buffers carved from the operand tiles the MMAs no longer need and written by TMA
-    // stores, which drain while the next round is computed.  e^b arrives by TMA over the
-    // A tile.
+    // stores, which drain while the next round is computed.  e^b arrives by TMA with the
+    // other inputs, in a tile of its own.
     const bool ready = ok && (ok = wait_bar(ctl, M_DV, 0)) && (ok = wait_bar(ctl, M_EB, 0));
     if (ready) tc_fence_after();
     const int et = threadIdx.x - 64;           // 0..255
@@ -305,7 +299,7 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
           const uint32_t off = sw128_offset(t, i0 + 8 * m, kC);
           const uint4 qv = *reinterpret_cast<const uint4*>(sm + C_QT + off);
           const uint4 kv = *reinterpret_cast<const uint4*>(sm + C_KT + off);
-          const uint4 ev = *reinterpret_cast<const uint4*>(sm + C_HS + off);
+          const uint4 ev = *reinterpret_cast<const uint4*>(sm + C_EB + off);
           const uint32_t qa[4] = {qv.x, qv.y, qv.z, qv.w};
           const uint32_t ka[4] = {kv.x, kv.y, kv.z, kv.w};
           const uint32_t ea[4] = {ev.x, ev.y, ev.z, ev.w};
