@@ -61,23 +61,22 @@ ALGO_BYTES_PER_TOKEN_HEAD = {
 # source changed since then reports "traffic": null.
 PROFILED_TRAFFIC = {
     # profiles/ncu_step_kernels_llama3_8b.md
-    "fwd_prep": {"bytes_per_token_head": 1508, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
-                "sha256": "2826c75940ae7f48a4adff9f324de002586116904f98fc86bbdf6b896b71edc6"},
-    "fwd_scan_tc": {"bytes_per_token_head": 542, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
-                   "sha256": "2826c75940ae7f48a4adff9f324de002586116904f98fc86bbdf6b896b71edc6"},
-    "fwd_chunk_tc": {"bytes_per_token_head": 1704, "source": "hybrid_gated_linear_gb300/csrc/k_fwd_chunk_tc.cu",
-                    "sha256": "21f428d924d56bcc371fbd35d5cd97de74ca01f12f23e09c0488733cf9c99f8d"},
-    "bwd_scan_tc": {"bytes_per_token_head": 540, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
-                   "sha256": "2826c75940ae7f48a4adff9f324de002586116904f98fc86bbdf6b896b71edc6"},
-    "bwd_chunk_tc": {"bytes_per_token_head": 3134, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
-                    "sha256": "de1faff4a8637d3c238ae54323079a468051cda31f42a494dde9241a1291ab2d"},
-    "bwd_suffix": {"bytes_per_token_head": 549, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
-                  "sha256": "de1faff4a8637d3c238ae54323079a468051cda31f42a494dde9241a1291ab2d"},
-    # window rows re-captured (kernel code as now; only the launch code changed since)
-    "win_bwd_q_tc": {"bytes_per_token_head": 1172, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
-                    "sha256": "151e07ea2f3bcefb27a7db74a71e2a1498cb372c2c334b0371405841cfa39806"},
-    "win_bwd_k_tc": {"bytes_per_token_head": 1874, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
-                    "sha256": "151e07ea2f3bcefb27a7db74a71e2a1498cb372c2c334b0371405841cfa39806"},
+    "fwd_prep": {"bytes_per_token_head": 1456, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
+               "sha256": "5c3bb8d989e13500e37fcc6f2ec2f970f8225ba963b4d45e414413cae69a9815"},
+    "fwd_scan_tc": {"bytes_per_token_head": 543, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
+                  "sha256": "5c3bb8d989e13500e37fcc6f2ec2f970f8225ba963b4d45e414413cae69a9815"},
+    "fwd_chunk_tc": {"bytes_per_token_head": 1701, "source": "hybrid_gated_linear_gb300/csrc/k_fwd_chunk_tc.cu",
+                   "sha256": "741ab27f7f940b9830371a9aeb487e27e26966b5bc2b89410397f1819963ccc7"},
+    "bwd_scan_tc": {"bytes_per_token_head": 538, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
+                  "sha256": "5c3bb8d989e13500e37fcc6f2ec2f970f8225ba963b4d45e414413cae69a9815"},
+    "bwd_chunk_tc": {"bytes_per_token_head": 3030, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
+                   "sha256": "340d928b091d4b79ccff6e711c922308b17ef9bc4edef70cafa9b3b75df7c58e"},
+    "bwd_suffix": {"bytes_per_token_head": 550, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
+                 "sha256": "340d928b091d4b79ccff6e711c922308b17ef9bc4edef70cafa9b3b75df7c58e"},
+    "win_bwd_q_tc": {"bytes_per_token_head": 1171, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
+                   "sha256": "151e07ea2f3bcefb27a7db74a71e2a1498cb372c2c334b0371405841cfa39806"},
+    "win_bwd_k_tc": {"bytes_per_token_head": 1879, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
+                   "sha256": "151e07ea2f3bcefb27a7db74a71e2a1498cb372c2c334b0371405841cfa39806"},
 }
 
 DECODE_BYTES_PER_UNIT = 2 * 65536 + 2 * 64 * 128 * 2 + 5 * 256 + 512 + 2 * 256 + 256
