@@ -285,49 +285,66 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
       tc_fence_after();
       const int nbatch = (ng + GB - 1) / GB;
       uint32_t z[GB][16];
+      // logits this row does not see are set to -inf once, as they are loaded, so that the
+      // max pass is a plain maximum and the exponent pass needs no test (2^-inf = 0)
       auto load_batch = [&](int b) {
 #pragma unroll
         for (int k = 0; k < GB; ++k)
           if (b * GB + k < ng) tmem_ld16(tl + G::TZ + zcol(b * GB + k), z[k]);
         tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < GB; ++k)
+          if (b * GB + k < ng) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (!vis(b * GB + k, e)) z[k][e] = 0xff800000u;
+          }
       };
-      float mx = -INFINITY;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       for (int b = 0; b < nbatch; ++b) {
         load_batch(b);
 #pragma unroll
         for (int k = 0; k < GB; ++k) {
           if (b * GB + k < ng) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              if (vis(b * GB + k, e)) mx = fmaxf(mx, __uint_as_float(z[k][e]));
+            for (int e = 0; e < 16; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(z[k][e]));
           }
         }
       }
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       const float mxs = mx * zs;
-      sum = 0.f;
+      float s2[2] = {0.f, 0.f};
       for (int b = 0; b < nbatch; ++b) {
         if (nbatch > 1) load_batch(b);
 #pragma unroll
         for (int k = 0; k < GB; ++k) {
           const int g = b * GB + k;
           if (g < ng) {
-            float pv[16];
+            // pairs of probabilities rounded once to bf16: the packed word is what the MMA
+            // reads and what the row sum adds up
+            uint32_t w[8];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float ex = vis(g, e) ? ex2_approx(fmaf(__uint_as_float(z[k][e]), zs, -mxs)) : 0.f;
-              pv[e] = __bfloat162float(__float2bfloat16_rn(ex));  // the value the MMA sees
-              sum += pv[e];
+            for (int e = 0; e < 8; ++e) {
+              const float e0 = ex2_approx(fmaf(__uint_as_float(z[k][2 * e]), zs, -mxs));
+              const float e1 = ex2_approx(fmaf(__uint_as_float(z[k][2 * e + 1]), zs, -mxs));
+              w[e] = pack_bf16x2(e0, e1);
+              s2[0] += __uint_as_float(w[e] << 16);
+              s2[1] += __uint_as_float(w[e] & 0xffff0000u);
             }
             if (g < nmeta) {
 #pragma unroll
               for (int e = 0; e < 16; ++e)
-                *reinterpret_cast<bf16*>(sm + G::PMT + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(pv[e]);
+                *reinterpret_cast<uint16_t*>(sm + G::PMT + sw128_offset(e, r, kMetaRows)) =
+                    (uint16_t)((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xffffu));
             } else {
-              store16_bf16(sm + G::KB, kC, r, 16 * (g_lo + g - nmeta), pv);
+              const int col = 16 * (g_lo + g - nmeta);
+              *reinterpret_cast<uint4*>(sm + G::KB + sw128_offset(r, col, kC)) = make_uint4(w[0], w[1], w[2], w[3]);
+              *reinterpret_cast<uint4*>(sm + G::KB + sw128_offset(r, col + 8, kC)) = make_uint4(w[4], w[5], w[6], w[7]);
             }
           }
         }
       }
+      sum = s2[0] + s2[1];
     }
     // band groups no row of this warp sees hold zeros (the tile still holds keys)
     for (int g = 0; g < BR / 16; ++g)
