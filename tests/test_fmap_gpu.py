@@ -236,3 +236,18 @@ def test_fused_forward_flags_gate_sums_out_of_range():
     x["log_gamma"] = np.full_like(x["log_gamma"], -2.0)  # chunk sums reach -256
     _, _, ws, _, _ = _run_fused(x, 64, 1.0, want_hf=False)
     assert lz.lizard_check_device_errors(ws) == 5  # LIZARD_ERR_DEVICE_CHECK
+
+
+def test_fused_forward_without_tokens_carries_h0():
+    import torch
+    import hybrid_gated_linear_gb300 as lz
+    dims = lz.lizard_dims(1, 2, 0, 128, 128, 4, lz.LIZARD_BF16, 0.0)
+    w = torch.zeros(2, 128, 64, dtype=torch.bfloat16, device="cuda")
+    mk = torch.zeros(2, 4, 128, dtype=torch.bfloat16, device="cuda")
+    h0 = torch.randn(1, 2, 128, 128, dtype=torch.float32, device="cuda")
+    hf = torch.empty_like(h0)
+    ws = torch.zeros(max(16, lz.lizard_fwd_workspace_bytes(dims, 64)), dtype=torch.uint8, device="cuda")
+    lz.lizard_attn_fwd_fmap(dims, None, None, w, w, None, None, None, None, mk, mk, 64, 1.0, None,
+                            h0, hf, ws)
+    assert lz.lizard_check_device_errors(ws) == 0
+    assert torch.equal(hf, h0)

@@ -45,12 +45,12 @@ def _run_bwd(x, W, h0, fwd_ws_from_forward):
     return {n: host(v) for n, v in g.items()}, launches
 
 
-@pytest.mark.parametrize("gate", ["slow", "bimodal"])
-def test_split_forward_matches_oracle(gate):
-    """B=1, H=2, L=3000: 24 chunks of 128 tokens for 8 scan CTAs, split in 3 segments;
-    y and h_final from a nonzero h0 against the oracle."""
-    import hybrid_gated_linear_gb300 as lz
-    B, H, L, d, W, M = 1, 2, 3000, 128, 64, 4
+@pytest.mark.parametrize("gate,L", [("slow", 3000), ("bimodal", 3000), ("plain", 2900)])
+def test_split_forward_matches_oracle(gate, L):
+    """B=1, H=2: L=3000 gives 24 chunks of 128 tokens for 8 scan CTAs, split in 3
+    segments of 8; L=2900 gives 23 chunks in segments of 12 and 11 with a ragged last
+    chunk.  y and h_final from a nonzero h0 against the oracle."""
+    B, H, d, W, M = 1, 2, 128, 64, 4
     x = synth.make_fwd_inputs(B, H, L, d, d, M, "bf16", gate, seed=800, with_dy=False)
     h0 = (0.1 * np.random.default_rng(801).standard_normal((B, H, d, d))).astype(np.float32)
     y, hf = gpu_fwd(x, W, "bf16", h0=h0, want_hf=True)
@@ -77,10 +77,11 @@ def test_split_forward_launches_the_join():
     assert counts == {3000: 5, 900: 3}, counts
 
 
-def test_split_backward_matches_oracle_with_and_without_the_forward_context():
+@pytest.mark.parametrize("L", [3000, 2900])
+def test_split_backward_matches_oracle_with_and_without_the_forward_context(L):
     """The adjoint scan alone (with the forward's context) and both scans (without) split;
     every gradient, d_h0 included, against the oracle, and the two runs bitwise equal."""
-    B, H, L, d, W, M = 1, 2, 3000, 128, 64, 4
+    B, H, d, W, M = 1, 2, 128, 64, 4
     x = synth.make_fwd_inputs(B, H, L, d, d, M, "bf16", "slow", seed=810, with_dy=True)
     h0 = (0.1 * np.random.default_rng(811).standard_normal((B, H, d, d))).astype(np.float32)
     a, na = _run_bwd(x, W, h0, fwd_ws_from_forward=False)
