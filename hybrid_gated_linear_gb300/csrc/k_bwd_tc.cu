@@ -393,8 +393,11 @@ __global__ void __launch_bounds__(kD) suffix_kernel(int L, int nc, float* dlg, c
     pdl_trigger();
     return;
   }
-  float carry = 0.f;
-  for (int c2 = nc - 1; c2 > c; --c2) carry += rtot[((size_t)bh * nc + c2) * kD + i];
+  // the later chunks' totals, in four independent sums so that their loads overlap
+  float cs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int c2 = c + 1; c2 < nc; ++c2) cs[(c2 - c - 1) & 3] += rtot[((size_t)bh * nc + c2) * kD + i];
+  const float carry = (cs[0] + cs[1]) + (cs[2] + cs[3]);
   const int t0 = c * kC, n = min(kC, L - t0);
   float* r = dlg + ((size_t)bh * L + t0) * kD + i;
 #pragma unroll 8
