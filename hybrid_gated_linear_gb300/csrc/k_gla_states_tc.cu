@@ -12,11 +12,12 @@
 //                       end (direction 1)
 //                         G_{nc-1} = 0,  G_{c-1} = diag(e^Gamma_c) G_c + Qt_c^T dY_c
 //                       stored as bf16 h_c and Gt_c = diag(e^Gamma_c) G_c; h_nc is h_final
-//                       and G_{-1} the adjoint of h0 (fp32).  One CTA per (b, h, 32 dv
-//                       columns, direction): warp 0 streams the chunks by TMA through a
-//                       4-deep ring, warp 1 issues one M=128 N=32 K=128 MMA per chunk into
-//                       one of 4 TMEM tiles, warps 2-5 (thread = state row) run the scan
-//                       in fp32 registers.
+//                       and G_{-1} the adjoint of h0 (fp32).  One CTA per (b, h, 64 or 32
+//                       dv columns, direction): warp 0 streams the chunks by TMA through a
+//                       ring of 4 (or 2) stages, warp 1 issues one M=128 N=64 (32) K=128
+//                       product per chunk into one TMEM tile per stage, and the scan warps
+//                       (thread = state row x 32 columns) run the recurrence in fp32
+//                       registers.
 #include "lizard_dev.cuh"
 #include "lizard_internal.h"
 #include "tc_pipe.cuh"
@@ -88,35 +89,42 @@ struct ScanMaps {
 };
 
 constexpr uint32_t kScanX = kC * kD * 2;  // 32 KB: Kt or Qt tile
-constexpr int kScanThreads = 6 * 32;
 constexpr int kGamAhead = 32;  // chunk decays fetched per refill by each scan row
 
-// SL value columns per CTA (32, 64 or 128) and kStages chunks in flight (TMA ring and
-// TMEM buffers).  The Y slice (V or dY) is a 64-byte-swizzled 32-column tile when SL = 32
-// and 128-byte-swizzled 64-column blocks otherwise.
+// SL value columns per CTA (32 or 64) and kStages chunks in flight (TMA ring and TMEM
+// buffers).  The Y slice (V or dY) is a 64-byte-swizzled 32-column tile when SL = 32 and a
+// 128-byte-swizzled 64-column block when SL = 64.  One scan warp per (TMEM lane quarter,
+// 32 columns): every scan thread carries 32 state columns of one row, whatever SL is.
+//
+// Each tcgen05 instruction the single MMA thread issues costs it on the order of 100 SM
+// cycles, whatever the tile's N: a chunk's eight K = 16 MMAs and its commit take ~0.4 us
+// and, with the copies' latency, set the pace of the chain.  One commit per chunk tells
+// both the producer (stage free) and the scan threads (accumulator full).
 template <int kStages, int SL>
 struct ScanCfg {
-  enum { S_FULL = 0, S_EMPTY = kStages, S_DFULL = 2 * kStages, S_DFREE = 3 * kStages,
-         S_DONE = 4 * kStages, S_COUNT };
+  enum { S_FULL = 0, S_DFULL = kStages, S_DFREE = 2 * kStages, S_DONE = 3 * kStages, S_COUNT };
+  static constexpr int kScanWarps = 4 * (SL / 32);
+  static constexpr int kThreads = (2 + kScanWarps) * 32;
   static constexpr uint32_t kY = kC * SL * 2;
   static constexpr uint32_t kStage = kScanX + kY;  // multiple of 1024
-  // each state row's next kGamAhead chunk decays, [kGamAhead][128] fp32
+  // each scan warp's rows' next kGamAhead chunk decays, [SL / 32][kGamAhead][128] fp32
   static constexpr uint32_t kGam = kStages * kStage;
-  static constexpr uint32_t kBars = kGam + kGamAhead * kD * 4;
+  static constexpr uint32_t kBars = kGam + (SL / 32) * kGamAhead * kD * 4;
   static constexpr size_t kSmem = kBars + 1024 + 1024;
   static constexpr uint32_t kTmemCols = kStages * SL <= 32 ? 32 : kStages * SL <= 64 ? 64
                                       : kStages * SL <= 128 ? 128 : kStages * SL <= 256 ? 256 : 512;
+  static_assert(SL == 32 || SL == 64, "slice width");
   static_assert(kStages * SL <= 512, "TMEM budget");
   static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
 template <int kStages, int SL>
-__global__ void __launch_bounds__(kScanThreads, 1)
+__global__ void __launch_bounds__(ScanCfg<kStages, SL>::kThreads, 1)
 scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc, int ndir,
             int dir0, int nseg, int cps, float* segf0, float* segf1) {
   using SC = ScanCfg<kStages, SL>;
-  enum { S_FULL = SC::S_FULL, S_EMPTY = SC::S_EMPTY, S_DFULL = SC::S_DFULL,
-         S_DFREE = SC::S_DFREE, S_DONE = SC::S_DONE, S_COUNT = SC::S_COUNT };
+  enum { S_FULL = SC::S_FULL, S_DFULL = SC::S_DFULL, S_DFREE = SC::S_DFREE,
+         S_DONE = SC::S_DONE, S_COUNT = SC::S_COUNT };
   constexpr int kSlicesT = kD / SL;
   constexpr uint32_t kScanBars = SC::kBars, kStageB = SC::kStage;
   extern __shared__ unsigned char smem_raw[];
@@ -135,7 +143,7 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S_COUNT; ++i)
-      mbar_init(&ctl->bar[i], (i >= S_DFREE && i < S_DFREE + kStages) ? 128u : 1u);
+      mbar_init(&ctl->bar[i], (i >= S_DFREE && i < S_DFREE + kStages) ? 32u * SC::kScanWarps : 1u);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -157,7 +165,8 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
       bool ok = true;
       for (int u = 0; u < nl && ok; ++u) {
         const int c = dir ? ce - 1 - u : cb + u, s = u % kStages, k = u / kStages;
-        if (k >= 1 && !(ok = wait_bar(ctl, S_EMPTY + s, (k - 1) & 1))) break;
+        // the stage is free once the MMAs of its previous chunk have completed
+        if (k >= 1 && !(ok = wait_bar(ctl, S_DFULL + s, (k - 1) & 1))) break;
         unsigned char* st = sm + s * kStageB;
         mbar_arrive_expect_tx(&ctl->bar[S_FULL + s], kStageB);
         tma_load_3d(st, mx, 0, c * kC, bh, &ctl->bar[S_FULL + s]);
@@ -183,19 +192,26 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
       // D[i][j] = sum_s X[s][i] Y[s][j]: A = X^T (MN-major), B = Y slice (MN-major)
       const uint32_t id = idesc_bf16(kD, SL, true, true);
       const uint32_t sbase = smem_u32(sm);
+      // stage 0's operand descriptors; k-step j of a stage adds j * 2048 bytes (16 token rows
+      // of 128 B) to A and j * kBStep to B (16 rows of the 64-byte-swizzled 32-column slice,
+      // or of the 128-byte-swizzled 64-column block)
+      constexpr uint32_t kBStep = SL == 32 ? 1024 : 2048;
+      const uint64_t a0 = desc_mn(sbase, kC, 0);
+      const uint64_t b0 = SL == 32 ? smem_desc(sbase + kScanX, kC * 64, 512, kSw64)
+                                   : desc_mn(sbase + kScanX, kC, 0);
       bool ok = true;
       for (int u = 0; u < nl && ok; ++u) {
         const int s = u % kStages, k = u / kStages;
         if (!(ok = wait_bar(ctl, S_FULL + s, k & 1))) break;
         if (k >= 1 && !(ok = wait_bar(ctl, S_DFREE + s, (k - 1) & 1))) break;
         tc_fence_after();
-        const uint32_t xb = sbase + s * kStageB, yb = xb + kScanX;
-        for (int j = 0; j < kC / 16; ++j) {
-          const uint64_t bdesc = SL == 32 ? smem_desc(yb + j * 1024, kC * 64, 512, kSw64)
-                                          : desc_mn(yb, kC, j);
-          mma_bf16(tmem + s * SL, desc_mn(xb, kC, j), bdesc, id, j > 0);
-        }
-        mma_commit(&ctl->bar[S_EMPTY + s]);
+        // descriptors differ only in the start address (16-byte units, low 14 bits)
+        const uint64_t soff = (uint64_t)((s * kStageB) >> 4);
+        const uint64_t ad = a0 + soff, bd = b0 + soff;
+        const uint32_t dt = tmem + s * SL;
+#pragma unroll
+        for (int j = 0; j < kC / 16; ++j)
+          mma_bf16(dt, ad + (uint64_t)(j * 2048 / 16), bd + (uint64_t)(j * kBStep / 16), id, j > 0);
         mma_commit(&ctl->bar[S_DFULL + s]);
       }
       if (!ok) ctl->abort = 1;
@@ -203,14 +219,17 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
       drain_bar(ctl, S_DONE, 1, globaltimer_ns());
     }
   } else {
-    const int qw = warp & 3;
+    // scan warp e: TMEM lane quarter warp % 4 (the quarter a warp may reach), columns
+    // 32 * (e / 4) .. + 31 of the slice
+    const int qw = warp & 3, cq = (warp - 2) >> 2;
     const int i = qw * 32 + lane;  // state row = TMEM lane
-    const uint32_t tl = tmem + ((uint32_t)(qw * 32) << 16);
-    float x[SL];
+    const int col = sl * SL + 32 * cq;  // first value column of this thread
+    const uint32_t tl = tmem + ((uint32_t)(qw * 32) << 16) + 32 * cq;
+    float x[32];
     if (dir == 0 && nseg == 1 && p.h0) {  // a split scan joins h0 in afterwards
-      const float4* src = reinterpret_cast<const float4*>(p.h0 + ((size_t)bh * kD + i) * kD + sl * SL);
+      const float4* src = reinterpret_cast<const float4*>(p.h0 + ((size_t)bh * kD + i) * kD + col);
 #pragma unroll
-      for (int k = 0; k < SL / 4; ++k) {
+      for (int k = 0; k < 8; ++k) {
         const float4 v = src[k];
         x[4 * k] = v.x;
         x[4 * k + 1] = v.y;
@@ -219,14 +238,14 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
       }
     } else {
 #pragma unroll
-      for (int k = 0; k < SL; ++k) x[k] = 0.f;
+      for (int k = 0; k < 32; ++k) x[k] = 0.f;
     }
     bf16* outb = dir ? p.gs : p.hs;
     bool ok = true;
     // The chunk decays sit on the scan's chain: each row fetches its next kGamAhead of them
     // with independent loads into its own column of shared memory (read back by the same
     // thread only), so a global load's latency is paid once per kGamAhead chunks.
-    float* gsm = reinterpret_cast<float*>(sm + SC::kGam);
+    float* gsm = reinterpret_cast<float*>(sm + SC::kGam) + cq * kGamAhead * kD;
     for (int u = 0; u < nl && ok; ++u) {
       const int c = dir ? ce - 1 - u : cb + u, s = u % kStages;
       if (u % kGamAhead == 0) {
@@ -243,29 +262,24 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
       const float g = expf(gsm[(u % kGamAhead) * kD + i]);
       if (!(ok = wait_bar(ctl, S_DFULL + s, (u / kStages) & 1))) break;
       tc_fence_after();
-      uint4* dst = reinterpret_cast<uint4*>(outb + (((size_t)bh * nc + c) * kD + i) * kD + sl * SL);
+      uint4* dst = reinterpret_cast<uint4*>(outb + (((size_t)bh * nc + c) * kD + i) * kD + col);
+      uint32_t d[32];
+      tmem_ld32(tl + s * SL, d);
+      tmem_ld_wait();
+      if (dir) {
 #pragma unroll
-      for (int g32 = 0; g32 < SL / 32; ++g32) {
-        uint32_t d[32];
-        tmem_ld32(tl + s * SL + 32 * g32, d);
-        tmem_ld_wait();
-        float* xs = x + 32 * g32;
-        if (dir) {
+        for (int k = 0; k < 32; ++k) x[k] *= g;
+      }
 #pragma unroll
-          for (int k = 0; k < 32; ++k) xs[k] *= g;
-        }
+      for (int k = 0; k < 4; ++k)
+        dst[k] = make_uint4(pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
+                            pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
+      if (dir) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          dst[4 * g32 + k] =
-              make_uint4(pack_bf16x2(xs[8 * k], xs[8 * k + 1]), pack_bf16x2(xs[8 * k + 2], xs[8 * k + 3]),
-                         pack_bf16x2(xs[8 * k + 4], xs[8 * k + 5]), pack_bf16x2(xs[8 * k + 6], xs[8 * k + 7]));
-        if (dir) {
+        for (int k = 0; k < 32; ++k) x[k] += __uint_as_float(d[k]);
+      } else {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) xs[k] += __uint_as_float(d[k]);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) xs[k] = g * (xs[k] + __uint_as_float(d[k]));
-        }
+        for (int k = 0; k < 32; ++k) x[k] = g * (x[k] + __uint_as_float(d[k]));
       }
       tc_fence_before();
       mbar_arrive(&ctl->bar[S_DFREE + s]);
@@ -278,9 +292,9 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
     else if (float* f = dir ? p.dh0 : p.hf)
       fin = f + (size_t)bh * kD * kD;
     if (ok && fin) {
-      float4* dst = reinterpret_cast<float4*>(fin + (size_t)i * kD + sl * SL);
+      float4* dst = reinterpret_cast<float4*>(fin + (size_t)i * kD + col);
 #pragma unroll
-      for (int k = 0; k < SL / 4; ++k) dst[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+      for (int k = 0; k < 8; ++k) dst[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
     }
   }
 
@@ -336,7 +350,7 @@ cudaError_t scan_variant(const GlaStatesArgs& a, bool states, bool adjoints, int
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SC::kSmem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(kScanThreads), SC::kSmem, s, m, a, nc, ndir, dir0,
+  return launch_pdl(kern, dim3(grid), dim3(SC::kThreads), SC::kSmem, s, m, a, nc, ndir, dir0,
                     nseg, cps, segf0, segf1);
 }
 
@@ -355,11 +369,10 @@ cudaError_t launch_gla_scan(const GlaStatesArgs& a, GlaScan which, cudaStream_t 
   }
   float* segf0 = nseg > 1 ? a.seg : nullptr;
   float* segf1 = nseg > 1 ? a.seg + (size_t)2 * a.BH * cap * kD * kD : nullptr;
-  // 32 value columns per CTA: measured against 64 and 128 (which read each Kt/Qt tile fewer
-  // times), the narrow slice keeps the per-chunk chain of every CTA shortest.
+  // 32 value columns per CTA (measured against 64: 26.5 -> 36 us per CTA on B=1, H=32,
+  // L=4096, with the MMA phase and the eight scan warps' epilogues both slower); five
+  // chunks in flight when the grid fits one wave, else two so that two CTAs share an SM
   trace_begin(adjoints ? "bwd_scan_tc" : "fwd_scan_tc", s);
-  // five chunks in flight when the grid fits one wave (measured against four: 27.9 -> 26.7
-  // us on B=1, H=32, L=4096), else two so that two CTAs share an SM
   cudaError_t e = a.BH * 4 * ndir * nseg <= ctas_per_wave(1)
                       ? scan_variant<5, 32>(a, states, adjoints, nc, nseg, cps, segf0, segf1, s)
                       : scan_variant<2, 32>(a, states, adjoints, nc, nseg, cps, segf0, segf1, s);
