@@ -279,7 +279,10 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
     if (ready) tc_fence_after();
     const int et = threadIdx.x - 64;           // 0..255
     const int scol = et & 31, seg = et >> 5;   // suffix pass: column of the round, 16-row segment
-    const bool issuer = et == 0;
+    // lane 0 of the first four epilogue warps each issue one of the round's four stores (a
+    // TMA issue costs its thread tens of nanoseconds; four warps issue side by side)
+    const int sidx = scol == 0 && seg < 4 ? seg : -1;
+    const CUtensorMap* smap = sidx == 0 ? &maps.dpq : sidx == 1 ? &maps.dpk : sidx == 2 ? &maps.dlg : &maps.dvo;
 #pragma unroll 1
     for (int R = 0; R < 4; ++R) {
       // buffer 0: dY tile + first half of V; buffer 1: second half of V + Gt tile
@@ -290,9 +293,10 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
       const int cl = 16 * hf;       // columns within the round
       const int i0 = 32 * R + cl;   // columns of the tile
       if (ready) {
-        uint32_t dq[16], dk[16];
+        uint32_t dq[16], dk[16], dv[16];
         tmem_ld16(tl + T_DQ + i0, dq);
         tmem_ld16(tl + T_DK + i0, dk);
+        tmem_ld16(tl + T_A + i0, dv);
         tmem_ld_wait();
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
@@ -323,9 +327,6 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
           *reinterpret_cast<float4*>(srr + sw128_offset_f32(t, cl + 8 * m + 4, kC)) =
               make_float4(rr[4], rr[5], rr[6], rr[7]);
         }
-        uint32_t dv[16];
-        tmem_ld16(tl + T_A + i0, dv);
-        tmem_ld_wait();
 #pragma unroll
         for (int m = 0; m < 4; ++m)
           *reinterpret_cast<float4*>(sdv + sw128_offset_f32(t, cl + 4 * m, kC)) =
@@ -333,12 +334,16 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
                           __uint_as_float(dv[4 * m + 2]), __uint_as_float(dv[4 * m + 3]));
       }
       named_sync(1, kEpiThreads);
-      // suffix sums of r down the chunk: 8 segments of 16 rows per column
+      // suffix sums of r down the chunk: 8 segments of 16 rows per column; the thread keeps
+      // its segment's 16 values in registers between the two passes
+      float rv[16];
       if (ready) {
         float part = 0.f;
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          part += *reinterpret_cast<const float*>(srr + sw128_offset_f32(16 * seg + u, scol, kC));
+        for (int u = 0; u < 16; ++u) {
+          rv[u] = *reinterpret_cast<const float*>(srr + sw128_offset_f32(16 * seg + u, scol, kC));
+          part += rv[u];
+        }
         red[seg * 32 + scol] = part;
       }
       named_sync(1, kEpiThreads);
@@ -349,26 +354,22 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
           if (s2 > seg) run += red[s2 * 32 + scol];
 #pragma unroll
         for (int u = 15; u >= 0; --u) {
-          float* q = reinterpret_cast<float*>(srr + sw128_offset_f32(16 * seg + u, scol, kC));
-          run += *q;
-          *q = run;
+          run += rv[u];
+          *reinterpret_cast<float*>(srr + sw128_offset_f32(16 * seg + u, scol, kC)) = run;
         }
         if (seg == 0) p.rtot[((size_t)bh * nc + c) * kD + 32 * R + scol] = run;
       }
       fence_proxy_async_smem();
       named_sync(1, kEpiThreads);
-      if (ready && issuer) {
+      if (ready && sidx >= 0) {
         // rows at or beyond L are clipped by the stores
-        tma_store_3d(&maps.dpq, sdq, 32 * R, t0, bh);
-        tma_store_3d(&maps.dpk, sdk, 32 * R, t0, bh);
-        tma_store_3d(&maps.dlg, srr, 32 * R, t0, bh);
-        tma_store_3d(&maps.dvo, sdv, 32 * R, t0, bh);
+        tma_store_3d(smap, sidx == 0 ? sdq : sidx == 1 ? sdk : sidx == 2 ? srr : sdv, 32 * R, t0, bh);
         bulk_commit();
-        bulk_wait_read_prev();  // the other buffer (round R-1) has been read
+        bulk_wait_read_prev();  // this thread's store of round R-1 (the other buffer) has been read
       }
       named_sync(1, kEpiThreads);
     }
-    if (ready && issuer) bulk_wait_read();
+    if (ready && sidx >= 0) bulk_wait_read();
     if (!ok) ctl->abort = 1;
   }
 
