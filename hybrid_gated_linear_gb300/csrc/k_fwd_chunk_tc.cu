@@ -272,10 +272,12 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
     const int nmeta = M > 0 ? 1 : 0;
     const int ng = nmeta + g_hi - g_lo + 1;
     auto zcol = [&](int g) { return g < nmeta ? 0 : 16 + 16 * (g_lo + g - nmeta); };
-    auto vis = [&](int g, int e) {
-      if (g < nmeta) return e < M;
-      const int b = 16 * (g_lo + g - nmeta) + e;
-      return b >= blo && b <= bhi;
+    // visible columns of group g as a 16-bit mask (bits lo .. hi of the group)
+    auto vmask = [&](int g) -> uint32_t {
+      if (g < nmeta) return (1u << M) - 1u;  // M <= 16
+      const int base = 16 * (g_lo + g - nmeta);
+      const int lo = max(blo - base, 0), hi = min(bhi - base, 15);
+      return hi < lo ? 0u : ((0xffffu >> (15 - hi)) >> lo) << lo;
     };
     // The window's logits are read from TMEM in batches of GB 16-column groups per wait;
     // with one batch (NP = 1) the exponent pass reuses the registers of the max pass.
@@ -283,7 +285,8 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
     float sum = 1.f;
     if (ok && (ok = wait_bar(ctl, F_ZF, 0))) {
       tc_fence_after();
-      const int nbatch = (ng + GB - 1) / GB;
+      // one batch always when NP = 1 (ng <= 7): a constant, so that the loops fold
+      const int nbatch = NP == 1 ? 1 : (ng + GB - 1) / GB;
       uint32_t z[GB][16];
       // logits this row does not see are set to -inf once, as they are loaded, so that the
       // max pass is a plain maximum and the exponent pass needs no test (2^-inf = 0)
@@ -295,9 +298,10 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
 #pragma unroll
         for (int k = 0; k < GB; ++k)
           if (b * GB + k < ng) {
+            const uint32_t mk = vmask(b * GB + k);
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              if (!vis(b * GB + k, e)) z[k][e] = 0xff800000u;
+              if (!(mk & (1u << e))) z[k][e] = 0xff800000u;
           }
       };
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
