@@ -283,6 +283,7 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
     // with one batch (NP = 1) the exponent pass reuses the registers of the max pass.
     constexpr int GB = NP == 1 ? 8 : 6;
     float sum = 1.f;
+    bool zeroed = false;
     if (ok && (ok = wait_bar(ctl, F_ZF, 0))) {
       tc_fence_after();
       // one batch always when NP = 1 (ng <= 7): a constant, so that the loops fold
@@ -294,6 +295,13 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
 #pragma unroll
         for (int k = 0; k < GB; ++k)
           if (b * GB + k < ng) tmem_ld16(tl + G::TZ + zcol(b * GB + k), z[k]);
+        if (b == 0 && !zeroed) {
+          // band groups no row of this warp sees hold zeros (the tile still holds keys);
+          // written while the TMEM loads are in flight (Z, which read the keys, is done)
+          for (int g = 0; g < BR / 16; ++g)
+            if (g < g_lo || g > g_hi) zero16_bf16(sm + G::KB, kC, r, 16 * g);
+          zeroed = true;
+        }
         tmem_ld_wait();
 #pragma unroll
         for (int k = 0; k < GB; ++k)
@@ -350,9 +358,6 @@ fwd_chunk_kernel(const __grid_constant__ FMaps maps, const FParams p) {
       }
       sum = s2[0] + s2[1];
     }
-    // band groups no row of this warp sees hold zeros (the tile still holds keys)
-    for (int g = 0; g < BR / 16; ++g)
-      if (g < g_lo || g > g_hi) zero16_bf16(sm + G::KB, kC, r, 16 * g);
     tc_fence_before();
     fence_proxy_async_smem();
     mbar_arrive(&ctl->bar[F_PR]);
