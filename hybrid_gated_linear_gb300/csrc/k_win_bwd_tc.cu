@@ -194,38 +194,65 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
     const int nmeta = M > 0 ? 1 : 0;
     const int ng = nmeta + g_hi - g_lo + 1;
     auto zcol = [&](int g) { return g < nmeta ? 0 : 16 + 16 * (g_lo + g - nmeta); };
-    auto vis = [&](int g, int e) {
-      if (g < nmeta) return e < M;
-      const int b = 16 * (g_lo + g - nmeta) + e;
-      return b >= blo && b <= bhi;
+    // visible columns of group g as a 16-bit mask (bits lo .. hi of the group)
+    auto vmask = [&](int g) -> uint32_t {
+      if (g < nmeta) return (1u << M) - 1u;  // M <= 16
+      const int base = 16 * (g_lo + g - nmeta);
+      const int lo = max(blo - base, 0), hi = min(bhi - base, 15);
+      return hi < lo ? 0u : ((0xffffu >> (15 - hi)) >> lo) << lo;
+    };
+    // The row's logits stay in registers for all three passes (at most one meta and six
+    // band groups when W <= 65), read from TMEM with a single wait; dP is read in two
+    // batches of four groups per pass.
+    constexpr int kNG = 7;
+    uint32_t z[kNG][16];
+    auto load_dp = [&](int h, uint32_t (&d)[4][16]) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (4 * h + k < kNG && 4 * h + k < ng) tmem_ld16(tl + TQ_DP + zcol(4 * h + k), d[k]);
+      tmem_ld_wait();
     };
     bool ok = wait_bar(ctl, Q_ZF, 0);
-    float mx = -INFINITY;
+    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     if (ok) {
       tc_fence_after();
-      for (int g = 0; g < ng; ++g) {
-        uint32_t z[16];
-        tmem_ld16(tl + TQ_Z + zcol(g), z);
-        tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          if (vis(g, e)) mx = fmaxf(mx, __uint_as_float(z[e]));
-      }
+      for (int g = 0; g < kNG; ++g)
+        if (g < ng) tmem_ld16(tl + TQ_Z + zcol(g), z[g]);
+      tmem_ld_wait();
+      // logits this row does not see become -inf: the maximum needs no test, and
+      // 2^-inf = 0 stands for them in the sums below
+#pragma unroll
+      for (int g = 0; g < kNG; ++g)
+        if (g < ng) {
+          const uint32_t mk = vmask(g);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            if (!(mk & (1u << e))) z[g][e] = 0xff800000u;
+            m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(z[g][e]));
+          }
+        }
     }
+    const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
     const float mxs = mx * zs;
     float sum = 0.f, sdp = 0.f;
     if (ok && (ok = wait_bar(ctl, Q_DPF, 0))) {
       tc_fence_after();
-      for (int g = 0; g < ng; ++g) {
-        uint32_t z[16], d[16];
-        tmem_ld16(tl + TQ_Z + zcol(g), z);
-        tmem_ld16(tl + TQ_DP + zcol(g), d);
-        tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float ex = vis(g, e) ? ex2_approx(fmaf(__uint_as_float(z[e]), zs, -mxs)) : 0.f;
-          sum += ex;
-          sdp = fmaf(ex, __uint_as_float(d[e]), sdp);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t d[4][16];
+        load_dp(h, d);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int g = 4 * h + k;
+          if (g < kNG && g < ng) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float ex = ex2_approx(fmaf(__uint_as_float(z[g][e]), zs, -mxs));
+              sum += ex;
+              sdp = fmaf(ex, __uint_as_float(d[k][e]), sdp);
+            }
+          }
         }
       }
     }
@@ -233,27 +260,32 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
     const float Dv = p.alpha * sdp / sum;
     unsigned char* dsb = sm + QS_VB;  // ds band tile, 128 rows x 192 columns
     if (ok) {
-      for (int g = 0; g < ng; ++g) {
-        uint32_t z[16], d[16];
-        tmem_ld16(tl + TQ_Z + zcol(g), z);
-        tmem_ld16(tl + TQ_DP + zcol(g), d);
-        tmem_ld_wait();
-        float ds[16], pp[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float pe = (valid && vis(g, e)) ? ex2_approx(fmaf(__uint_as_float(z[e]), zs, -lse2)) : 0.f;
-          pp[e] = pe;
-          ds[e] = pe * fmaf(p.alpha, __uint_as_float(d[e]), -Dv);
-        }
-        if (g < nmeta) {
-          // transposed meta tiles: row m, column r
+      for (int h = 0; h < 2; ++h) {
+        uint32_t d[4][16];
+        load_dp(h, d);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            *reinterpret_cast<bf16*>(sm + QS_DSM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(ds[e]);
-            *reinterpret_cast<bf16*>(sm + QS_PM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(pp[e]);
+        for (int k = 0; k < 4; ++k) {
+          const int g = 4 * h + k;
+          if (g < kNG && g < ng) {
+            float ds[16], pp[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float pe = valid ? ex2_approx(fmaf(__uint_as_float(z[g][e]), zs, -lse2)) : 0.f;
+              pp[e] = pe;
+              ds[e] = pe * fmaf(p.alpha, __uint_as_float(d[k][e]), -Dv);
+            }
+            if (g < nmeta) {
+              // transposed meta tiles: row m, column r
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                *reinterpret_cast<bf16*>(sm + QS_DSM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(ds[e]);
+                *reinterpret_cast<bf16*>(sm + QS_PM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(pp[e]);
+              }
+            } else {
+              store16_bf16(dsb, kB, r, 16 * (g_lo + g - nmeta), ds);
+            }
           }
-        } else {
-          store16_bf16(dsb, kB, r, 16 * (g_lo + g - nmeta), ds);
         }
       }
     }
