@@ -493,22 +493,44 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
     bool ok = wait_bar(ctl, K_SF, 0);
     if (ok) {
       tc_fence_after();
-      for (int g = g_lo; g <= g_hi; ++g) {
-        uint32_t s[16], d[16];
-        tmem_ld16(tl + TK_S + 16 * g, s);
-        tmem_ld16(tl + TK_DP + 16 * g, d);
-        tmem_ld_wait();
-        float pp[16], ds[16];
+      // at most six 16-column groups (W <= 65); the next group's TMEM loads are in flight
+      // while this one is worked on
+      constexpr int kNG = 7;
+      const int ng = g_hi - g_lo + 1;
+      uint32_t sv[2][16], dv[2][16];
+      tmem_ld16(tl + TK_S + 16 * g_lo, sv[0]);
+      tmem_ld16(tl + TK_DP + 16 * g_lo, dv[0]);
+      tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int u = 16 * g + e;
-          const bool vis = valid && u >= jr && u <= jr + W - 1;
-          const float pe = vis ? ex2_approx(fmaf(__uint_as_float(s[e]), zs, -rl[u])) : 0.f;
-          pp[e] = pe;
-          ds[e] = pe * fmaf(p.alpha, __uint_as_float(d[e]), -rd[u]);
+      for (int k = 0; k < kNG; ++k) {
+        if (k < ng) {
+          const int g = g_lo + k;
+          if (k + 1 < ng) {
+            tmem_ld16(tl + TK_S + 16 * (g + 1), sv[(k + 1) & 1]);
+            tmem_ld16(tl + TK_DP + 16 * (g + 1), dv[(k + 1) & 1]);
+          }
+          // columns of the group that see this key: bits lo .. hi
+          const int lo = max(jr - 16 * g, 0), hi = min(jr + W - 1 - 16 * g, 15);
+          const uint32_t mk = (!valid || hi < lo) ? 0u : ((0xffffu >> (15 - hi)) >> lo) << lo;
+          float rlv[16], rdv[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 a4 = reinterpret_cast<const float4*>(rl + 16 * g)[q];
+            const float4 b4 = reinterpret_cast<const float4*>(rd + 16 * g)[q];
+            rlv[4 * q] = a4.x; rlv[4 * q + 1] = a4.y; rlv[4 * q + 2] = a4.z; rlv[4 * q + 3] = a4.w;
+            rdv[4 * q] = b4.x; rdv[4 * q + 1] = b4.y; rdv[4 * q + 2] = b4.z; rdv[4 * q + 3] = b4.w;
+          }
+          float pp[16], ds[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float pe = (mk & (1u << e)) ? ex2_approx(fmaf(__uint_as_float(sv[k & 1][e]), zs, -rlv[e])) : 0.f;
+            pp[e] = pe;
+            ds[e] = pe * fmaf(p.alpha, __uint_as_float(dv[k & 1][e]), -rdv[e]);
+          }
+          store16_bf16(pt, kB, jr, 16 * g, pp);
+          store16_bf16(dst, kB, jr, 16 * g, ds);
+          tmem_ld_wait();
         }
-        store16_bf16(pt, kB, jr, 16 * g, pp);
-        store16_bf16(dst, kB, jr, 16 * g, ds);
       }
     }
     for (int g = 0; g < kBand / 16; ++g) {
