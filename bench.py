@@ -61,22 +61,22 @@ ALGO_BYTES_PER_TOKEN_HEAD = {
 # source changed since then reports "traffic": null.
 PROFILED_TRAFFIC = {
     # profiles/ncu_step_kernels_llama3_8b.md
-    "fwd_prep": {"bytes_per_token_head": 1456, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
-               "sha256": "5c3bb8d989e13500e37fcc6f2ec2f970f8225ba963b4d45e414413cae69a9815"},
-    "fwd_scan_tc": {"bytes_per_token_head": 543, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
-                  "sha256": "5c3bb8d989e13500e37fcc6f2ec2f970f8225ba963b4d45e414413cae69a9815"},
-    "fwd_chunk_tc": {"bytes_per_token_head": 1701, "source": "hybrid_gated_linear_gb300/csrc/k_fwd_chunk_tc.cu",
-                   "sha256": "741ab27f7f940b9830371a9aeb487e27e26966b5bc2b89410397f1819963ccc7"},
-    "bwd_scan_tc": {"bytes_per_token_head": 538, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
-                  "sha256": "5c3bb8d989e13500e37fcc6f2ec2f970f8225ba963b4d45e414413cae69a9815"},
-    "bwd_chunk_tc": {"bytes_per_token_head": 3030, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
-                   "sha256": "340d928b091d4b79ccff6e711c922308b17ef9bc4edef70cafa9b3b75df7c58e"},
-    "bwd_suffix": {"bytes_per_token_head": 550, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
-                 "sha256": "340d928b091d4b79ccff6e711c922308b17ef9bc4edef70cafa9b3b75df7c58e"},
-    "win_bwd_q_tc": {"bytes_per_token_head": 1171, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
-                   "sha256": "151e07ea2f3bcefb27a7db74a71e2a1498cb372c2c334b0371405841cfa39806"},
-    "win_bwd_k_tc": {"bytes_per_token_head": 1879, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
-                   "sha256": "151e07ea2f3bcefb27a7db74a71e2a1498cb372c2c334b0371405841cfa39806"},
+    "fwd_prep": {"bytes_per_token_head": 1455, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
+               "sha256": "81bf37211c65e637157ac9a4edeae0f8716981c526c4ea4bb4e69d10acf57409"},
+    "fwd_scan_tc": {"bytes_per_token_head": 541, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
+                  "sha256": "81bf37211c65e637157ac9a4edeae0f8716981c526c4ea4bb4e69d10acf57409"},
+    "fwd_chunk_tc": {"bytes_per_token_head": 1703, "source": "hybrid_gated_linear_gb300/csrc/k_fwd_chunk_tc.cu",
+                   "sha256": "632e7a89c2eb4b97d1e0c0ccaf49ea068a76f68e7ab3209b85a4e543df883d60"},
+    "bwd_scan_tc": {"bytes_per_token_head": 541, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
+                  "sha256": "81bf37211c65e637157ac9a4edeae0f8716981c526c4ea4bb4e69d10acf57409"},
+    "bwd_chunk_tc": {"bytes_per_token_head": 3052, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
+                   "sha256": "cffaffb1a8cad5556498febfe864e690d133a844031754264c8b140febbee8fc"},
+    "bwd_suffix": {"bytes_per_token_head": 549, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
+                 "sha256": "cffaffb1a8cad5556498febfe864e690d133a844031754264c8b140febbee8fc"},
+    "win_bwd_q_tc": {"bytes_per_token_head": 1170, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
+                   "sha256": "7ec0ebd48d5bb82652fc88fdc08b4afe070194fe483214165237362664fd14bb"},
+    "win_bwd_k_tc": {"bytes_per_token_head": 1884, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
+                   "sha256": "7ec0ebd48d5bb82652fc88fdc08b4afe070194fe483214165237362664fd14bb"},
 }
 
 DECODE_BYTES_PER_UNIT = 2 * 65536 + 2 * 64 * 128 * 2 + 5 * 256 + 512 + 2 * 256 + 256
