@@ -188,10 +188,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecArgs a) {
 //  * decode_gla_kernel streams the fp32 state (128 KiB of the 166 KiB a unit moves):
 //    every thread issues its sixteen 16-byte state loads before anything else, three
 //    CTAs share an SM, and y_gla goes to y.
-//  * decode_win_kernel stages the two rings in shared memory, computes the window
-//    softmax (8 lanes per key, lanes interleaved over dimensions so the shared-memory
-//    reads are conflict-free), adds alpha * y_win into y, writes the new token into its
-//    slot and advances pos (last CTA of each sequence).
+//  * decode_win_kernel stages the two rings in shared memory (keys and values in two
+//    copy groups), computes the window softmax (8 lanes per key, lanes interleaved over
+//    dimensions so the shared-memory reads are conflict-free), adds alpha * y_win into y,
+//    writes the new token into its slot and advances pos (last CTA of each sequence).
+//    It is launched as a programmatic dependent of decode_gla_kernel, whose outputs it
+//    reads only after griddepcontrol.wait: its ring copies run during the state pass's
+//    tail (a 64 x 32 step measured 67 -> 62 us).
 // ------------------------------------------------------------------------------------
 constexpr int kSplitMaxW = 128;
 constexpr int kWinThreads = 256;
@@ -213,6 +216,9 @@ __global__ void __launch_bounds__(kThreads, 3) decode_gla_kernel(DecArgs a) {
 #pragma unroll
   for (int i = 0; i < RPT; ++i)
     hv[i] = *reinterpret_cast<const float4*>(h + (size_t)(rg + RG * i) * DV + 4 * cg);
+  // the window kernel (launched next) reads nothing this kernel writes before its
+  // griddepcontrol.wait: let it start staging its rings during this kernel's tail
+  pdl_trigger();
   const T* pq = static_cast<const T*>(a.pq) + (size_t)u * DK;
   const T* pk = static_cast<const T*>(a.pk) + (size_t)u * DK;
   const float* lg = a.lg + (size_t)u * DK;
@@ -262,9 +268,11 @@ template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kWinThreads) decode_win_kernel(DecArgs a) {
   extern __shared__ __align__(128) unsigned char wsm[];
   const int W = a.W, M = a.M;
-  // keys: W ring rows then M meta rows; values likewise, so one row index serves both
-  T* skey = reinterpret_cast<T*>(wsm);            // [W + M][DK]
-  T* sval = skey + (size_t)(W + M) * DK;          // [W + M][DV]
+  // keys: W ring rows, M meta rows, then the new token's row; values likewise, so one
+  // row index serves both.  The new token has a row of its own, which no ring copy
+  // targets, so it needs no ordering against them.
+  T* skey = reinterpret_cast<T*>(wsm);            // [W + M + 1][DK]
+  T* sval = skey + (size_t)(W + M + 1) * DK;      // [W + M + 1][DV]
   __shared__ __align__(16) float s_q[DK];
   __shared__ float s_z[kMaxM + kSplitMaxW];
   __shared__ int s_row[kMaxM + kSplitMaxW];
@@ -286,6 +294,7 @@ __global__ void __launch_bounds__(kWinThreads) decode_win_kernel(DecArgs a) {
     for (int e = tid; e < W * KC; e += kWinThreads) cp_async16(skey + e * (16 / sizeof(T)), kr + e * (16 / sizeof(T)));
     for (int e = tid; e < M * KC; e += kWinThreads)
       cp_async16(skey + (size_t)W * DK + e * (16 / sizeof(T)), mkp + e * (16 / sizeof(T)));
+    asm volatile("cp.async.commit_group;" ::: "memory");  // keys: the logits need only these
     for (int e = tid; e < W * VC; e += kWinThreads) cp_async16(sval + e * (16 / sizeof(T)), vr + e * (16 / sizeof(T)));
     for (int e = tid; e < M * VC; e += kWinThreads)
       cp_async16(sval + (size_t)W * DV + e * (16 / sizeof(T)), mvp + e * (16 / sizeof(T)));
@@ -293,30 +302,29 @@ __global__ void __launch_bounds__(kWinThreads) decode_win_kernel(DecArgs a) {
   }
   const T* qg = static_cast<const T*>(a.q) + (size_t)u * DK;
   T* y = static_cast<T*>(a.y) + (size_t)u * DV;
-  const float ygla = tid < DV ? ld_f(y + tid) : 0.f;  // y_gla from the previous kernel
-  for (int d = tid; d < DK; d += kWinThreads) s_q[d] = ld_f(qg + d);
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  const int nrow = W + M;  // the new token's row
+  for (int d = tid; d < DK; d += kWinThreads) {
+    s_q[d] = ld_f(qg + d);
+    skey[(size_t)nrow * DK + d] = kg[d];
+  }
+  for (int c = tid; c < DV; c += kWinThreads) sval[(size_t)nrow * DV + c] = vg[c];
   __syncthreads();
   const int64_t p = s_pos;
   const int slot = (int)(p % W);
-  // the new token replaces its slot, in shared memory and in the global ring
-  for (int d = tid; d < DK; d += kWinThreads) {
-    skey[(size_t)slot * DK + d] = kg[d];
-    kr[(size_t)slot * DK + d] = kg[d];
-  }
-  for (int c = tid; c < DV; c += kWinThreads) {
-    sval[(size_t)slot * DV + c] = vg[c];
-    vr[(size_t)slot * DV + c] = vg[c];
-  }
+  // the new token replaces its slot in the global ring (the slot's old token is outside
+  // the window, so the copy of it in shared memory is never read)
+  for (int d = tid; d < DK; d += kWinThreads) kr[(size_t)slot * DK + d] = kg[d];
+  for (int c = tid; c < DV; c += kWinThreads) vr[(size_t)slot * DV + c] = vg[c];
   const int64_t t_lo = p - W + 1 > 0 ? p - W + 1 : 0;
   const int nkeys = M + (int)(p - t_lo + 1);
   // row of key j: meta keys first (rows W..W+M-1), then window token t_lo + i at slot
-  // (t_lo + i) mod W, computed as one wrap of s_lo + i
+  // (t_lo + i) mod W, computed as one wrap of s_lo + i; the newest token (p) in its own row
   const int s_lo = (int)(t_lo % W);
   for (int j = tid; j < nkeys; j += kWinThreads) {
     const int i = j - M, r = s_lo + i;
-    s_row[j] = j < M ? W + j : (r >= W ? r - W : r);
+    s_row[j] = j < M ? W + j : (j == nkeys - 1 ? nrow : (r >= W ? r - W : r));
   }
+  asm volatile("cp.async.wait_group 1;" ::: "memory");  // this thread's key copies
   __syncthreads();
   {
     // logits: 8 lanes per key, lane l8 takes dimensions {4*l8 + 32*i}
@@ -357,6 +365,7 @@ __global__ void __launch_bounds__(kWinThreads) decode_win_kernel(DecArgs a) {
     const float inv = 1.f / sum;
     for (int j = lane; j < nkeys; j += 32) s_z[j] *= inv;
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");  // this thread's value copies
   __syncthreads();
   constexpr int NP = kWinThreads / DV > 0 ? kWinThreads / DV : 1;  // key partitions
   {
@@ -375,11 +384,14 @@ __global__ void __launch_bounds__(kWinThreads) decode_win_kernel(DecArgs a) {
     }
   }
   __syncthreads();
+  // y_gla comes from the GLA kernel launched just before this one (programmatic
+  // dependent launch: everything above overlaps that kernel's tail)
+  pdl_wait();
   for (int c = tid; c < DV; c += kWinThreads) {
     float ys = 0.f;
 #pragma unroll
     for (int r = 0; r < NP; ++r) ys += s_part[r][c];
-    y[c] = cvt_out<T>(ygla + a.alpha * ys);
+    y[c] = cvt_out<T>(ld_f(y + c) + a.alpha * ys);
   }
   __syncthreads();
   if (tid == 0) {
@@ -403,13 +415,14 @@ cudaError_t launch_typed(const DecArgs& a, cudaStream_t s, int* launches) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++*launches;
-    const size_t smem = (size_t)(a.W + a.M) * 2 * D * sizeof(T);
+    const size_t smem = (size_t)(a.W + a.M + 1) * 2 * D * sizeof(T);
     e = cudaFuncSetAttribute(decode_win_kernel<T, D, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
     trace_begin("decode_win", s);
-    decode_win_kernel<T, D, D><<<a.N * a.H, kWinThreads, smem, s>>>(a);
+    e = launch_pdl(decode_win_kernel<T, D, D>, dim3(a.N * a.H), dim3(kWinThreads), smem, s, a);
     trace_end(s);
+    if (e != cudaSuccess) return e;
   } else {
     trace_begin("decode", s);
     decode_kernel<T, D, D><<<a.N * a.H, kThreads, 0, s>>>(a);
