@@ -13,7 +13,10 @@ using bf16 = __nv_bfloat16;
 // the grid launched before this one on the stream has completed and its memory is
 // visible (a no-op without such a dependency); pdl_trigger() lets the next grid start its
 // CTAs once every CTA of this grid has called it or exited.  Every kernel launched with
-// launch_pdl calls pdl_wait() before it reads anything an earlier kernel wrote.
+// launch_pdl calls pdl_wait() before it reads anything the grid launched just before it
+// may still be writing.  Data that grid never writes, and that was complete before that
+// grid was launched (by an ordinary stream dependency), may be read earlier: the decode
+// window kernel stages its rings that way.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
