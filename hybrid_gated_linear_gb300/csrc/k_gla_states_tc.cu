@@ -97,9 +97,10 @@ constexpr int kGamAhead = 32;  // chunk decays fetched per refill by each scan r
 // 32 columns): every scan thread carries 32 state columns of one row, whatever SL is.
 //
 // Each tcgen05 instruction the single MMA thread issues costs it on the order of 100 SM
-// cycles, whatever the tile's N: a chunk's eight K = 16 MMAs and its commit take ~0.4 us
-// and, with the copies' latency, set the pace of the chain.  One commit per chunk tells
-// both the producer (stage free) and the scan threads (accumulator full).
+// cycles, whatever the tile's N: a chunk's eight K = 16 MMAs and its commit take ~0.4 us,
+// the pace of the chain when the operands are in L2; from DRAM the copies set it.  One
+// commit per chunk tells both the producer (stage free) and the scan threads
+// (accumulator full).
 template <int kStages, int SL>
 struct ScanCfg {
   enum { S_FULL = 0, S_DFULL = kStages, S_DFREE = 2 * kStages, S_DONE = 3 * kStages, S_COUNT };
