@@ -62,13 +62,13 @@ ALGO_BYTES_PER_TOKEN_HEAD = {
 PROFILED_TRAFFIC = {
     # profiles/ncu_step_kernels_llama3_8b.md
     "fwd_prep": {"bytes_per_token_head": 1455, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
-               "sha256": "fddf72f4765f37b25befb77bb218d1eb1d5ed212d59bff1f7a8fe1e292f32bbc"},
+               "sha256": "2c9e1070d71be0a0efe6535b2264d9e75664ab6847f4766b7ca3fc3b780ccd0c"},
     "fwd_scan_tc": {"bytes_per_token_head": 541, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
-                  "sha256": "fddf72f4765f37b25befb77bb218d1eb1d5ed212d59bff1f7a8fe1e292f32bbc"},
+                  "sha256": "2c9e1070d71be0a0efe6535b2264d9e75664ab6847f4766b7ca3fc3b780ccd0c"},
     "fwd_chunk_tc": {"bytes_per_token_head": 1703, "source": "hybrid_gated_linear_gb300/csrc/k_fwd_chunk_tc.cu",
                    "sha256": "632e7a89c2eb4b97d1e0c0ccaf49ea068a76f68e7ab3209b85a4e543df883d60"},
     "bwd_scan_tc": {"bytes_per_token_head": 541, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
-                  "sha256": "fddf72f4765f37b25befb77bb218d1eb1d5ed212d59bff1f7a8fe1e292f32bbc"},
+                  "sha256": "2c9e1070d71be0a0efe6535b2264d9e75664ab6847f4766b7ca3fc3b780ccd0c"},
     "bwd_chunk_tc": {"bytes_per_token_head": 3052, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
                    "sha256": "cffaffb1a8cad5556498febfe864e690d133a844031754264c8b140febbee8fc"},
     "bwd_suffix": {"bytes_per_token_head": 549, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",

@@ -12,12 +12,12 @@
 //                       end (direction 1)
 //                         G_{nc-1} = 0,  G_{c-1} = diag(e^Gamma_c) G_c + Qt_c^T dY_c
 //                       stored as bf16 h_c and Gt_c = diag(e^Gamma_c) G_c; h_nc is h_final
-//                       and G_{-1} the adjoint of h0 (fp32).  One CTA per (b, h, 64 or 32
-//                       dv columns, direction): warp 0 streams the chunks by TMA through a
-//                       ring of 4 (or 2) stages, warp 1 issues one M=128 N=64 (32) K=128
-//                       product per chunk into one TMEM tile per stage, and the scan warps
-//                       (thread = state row x 32 columns) run the recurrence in fp32
-//                       registers.
+//                       and G_{-1} the adjoint of h0 (fp32).  One CTA per (b, h, 32 dv
+//                       columns, direction): warp 0 streams the chunks by TMA through a
+//                       ring of 5 (or, two CTAs to an SM, 2) stages, warp 1 issues one
+//                       M=128 N=32 K=128 product per chunk into one TMEM tile per stage,
+//                       and the scan warps (thread = state row x 32 columns) run the
+//                       recurrence in fp32 registers.
 #include "lizard_dev.cuh"
 #include "lizard_internal.h"
 #include "tc_pipe.cuh"
