@@ -21,20 +21,14 @@ namespace {
 constexpr int kD = 128;
 constexpr int kS = kD * kD;
 
-// Sum of gam[c][k] over chunks [c0, c1) of one unit, split over the 32 lanes of a warp
-// (lane j takes c0 + j, c0 + j + 32, ...) and reduced in a fixed butterfly order; every
-// lane returns the total.
-__device__ __forceinline__ float warp_gate_sum(const float* gam, size_t row0, int c0, int c1, int k) {
-  const int lane = threadIdx.x & 31;
-  float acc = 0.f;
-  for (int c = c0 + lane; c < c1; c += 32) acc += gam[(row0 + c) * kD + k];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  return acc;
-}
-
 // One thread per (unit, row k, four columns): the 32 threads of a row form one warp.  The
-// segments are walked in order.
+// segments are walked in order, in batches of kJB: a batch's gate sums and partial states
+// do not depend on the running state, so all of their loads are issued before the walk
+// uses any of them.  The gate sum of segment s over its chunks [c0, c1) is split over
+// the 32 lanes (lane j adds c0 + j, c0 + j + 32, ... in that order) and reduced in a
+// fixed butterfly order.
+constexpr int kJB = 8;
+
 __global__ void __launch_bounds__(256) seg_join_kernel(int nc, int nseg, int cps, int dir,
                                                        const float* __restrict__ gam,
                                                        const float* __restrict__ segf,
@@ -42,18 +36,48 @@ __global__ void __launch_bounds__(256) seg_join_kernel(int nc, int nseg, int cps
                                                        const float* __restrict__ h0,
                                                        float* __restrict__ fin) {
   const int bh = blockIdx.y, e = blockIdx.x * blockDim.x + threadIdx.x;
-  const int k = e >> 5, v = (e & 31) * 4;
+  const int k = e >> 5, v = (e & 31) * 4, lane = threadIdx.x & 31;
   pdl_wait();
   const size_t un = (size_t)bh * nseg, off = (size_t)k * kD + v;
+  const float* gk = gam + (size_t)bh * nc * kD + k;  // gam of chunk c, row k: gk[c * kD]
   float4 H = make_float4(0.f, 0.f, 0.f, 0.f);
   if (dir == 0 && h0) H = *reinterpret_cast<const float4*>(h0 + (size_t)bh * kS + off);
-  for (int t = 0; t < nseg; ++t) {
-    const int s = dir ? nseg - 1 - t : t;
-    *reinterpret_cast<float4*>(segh + (un + s) * kS + off) = H;
-    const float G = warp_gate_sum(gam, (size_t)bh * nc, s * cps, min(nc, (s + 1) * cps), k);
-    const float f = expf(G);
-    const float4 F = *reinterpret_cast<const float4*>(segf + (un + s) * kS + off);
-    H = make_float4(fmaf(f, H.x, F.x), fmaf(f, H.y, F.y), fmaf(f, H.z, F.z), fmaf(f, H.w, F.w));
+  for (int t0 = 0; t0 < nseg; t0 += kJB) {
+    float G[kJB];
+    float4 F[kJB];
+#pragma unroll
+    for (int b = 0; b < kJB; ++b) {
+      const int t = t0 + b;
+      const int s = dir ? nseg - 1 - t : t;
+      const int c0 = s * cps, c1 = min(nc, c0 + cps);
+      const bool live = t < nseg;
+      // the first two chunks of each lane as straight-line loads, the rest in a loop
+      const int ca = c0 + lane, cb = ca + 32;
+      const float va = live && ca < c1 ? gk[(size_t)ca * kD] : 0.f;
+      const float vb = live && cb < c1 ? gk[(size_t)cb * kD] : 0.f;
+      F[b] = live ? *reinterpret_cast<const float4*>(segf + (un + s) * kS + off)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      float acc = va + vb;
+      if (live)
+        for (int c = cb + 32; c < c1; c += 32) acc += gk[(size_t)c * kD];
+      G[b] = acc;
+    }
+#pragma unroll
+    for (int b = 0; b < kJB; ++b) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) G[b] += __shfl_xor_sync(0xffffffffu, G[b], o);
+    }
+#pragma unroll
+    for (int b = 0; b < kJB; ++b) {
+      const int t = t0 + b;
+      if (t < nseg) {
+        const int s = dir ? nseg - 1 - t : t;
+        *reinterpret_cast<float4*>(segh + (un + s) * kS + off) = H;
+        const float f = expf(G[b]);
+        H = make_float4(fmaf(f, H.x, F[b].x), fmaf(f, H.y, F[b].y), fmaf(f, H.z, F[b].z),
+                        fmaf(f, H.w, F[b].w));
+      }
+    }
   }
   if (fin) *reinterpret_cast<float4*>(fin + (size_t)bh * kS + off) = H;
   pdl_trigger();
