@@ -1,17 +1,23 @@
-// k_bwd_simt.cu -- backward pass on CUDA cores (fp32 FMA), any dtype.
+// k_bwd_simt.cu -- backward pass on CUDA cores (fp32 FMA), any dtype, and the exact
+// recomputation of the tensor-core backward's "wide" chunks.
 //
-// The pages give no backward formulas; these are the exact adjoints of the chunkwise
-// forward (see k_fwd_simt.cu).  Per chunk (C tokens, b chunk-local cumsum, Gamma its
-// last value, Qt = phi_q exp(b), Kt = phi_k exp(-b), h_prev the state at the chunk
-// start, G the adjoint of the state at the chunk end coming from later chunks):
-//   A[t][s] = dy_t . v_s,   P[t][s] = Qt_t . Kt_s          (s <= t)
-//   dQt_t = h_prev dy_t + sum_{s<=t} A[t][s] Kt_s          d_phi_q = dQt * exp(b)
-//   dKt_s = sum_{t>=s} A[t][s] Qt_t + exp(Gamma) (.) (G v_s)  d_phi_k = dKt * exp(-b)
-//   dv_s  = sum_{t>=s} P[t][s] dy_t + (Kt_s (.) exp(Gamma))^T G
-//   G    <- diag(exp(Gamma)) G + Qt^T dY                     (moving one chunk back)
-//   d log_gamma_t = sum_{t'>=t} (phi_q (.) d_phi_q - phi_k (.) d_phi_k)_{t'}
-// (the gate enters only through cumulative sums b, and d/db of Qt, Kt gives the
-// per-token term).  After the walk G is the adjoint of h0.
+// The pages give no backward formulas; these are the exact adjoints of the recurrence
+// the forward computes (papernotes.org note on Lizard, 关键设计;
+// "Lizard", arXiv 2507.09025, Preliminaries: recurrent form)
+//   h_t = diag(gamma_t) h_{t-1} + phi_k_t v_t^T,   y_t = phi_q_t^T h_t,   gamma_t = e^{log gamma_t}.
+// GLA branch, one CTA per (b, h) with the whole dk x dv state in registers (warp w: state
+// rows [w K, (w+1) K), K = dk / 16; lane: value columns lane + 32 j), two walks:
+//   forward:  h_t as above;                      d phi_q_t = h_t dy_t
+//   reverse:  dh_t = phi_q_t dy_t^T + diag(gamma_{t+1}) dh_{t+1}   (dh after the last
+//             token = 0, or the adjoint coming from later tokens);
+//             d phi_k_t = dh_t v_t,   dv_t = dh_t^T phi_k_t (the GLA part of dv)
+//   d log gamma_t = sum_{t' >= t} (phi_q (.) d phi_q - phi_k (.) d phi_k)_{t'}
+// The last line holds because log gamma_t enters every later state only through the
+// cumulative log decay, which multiplies the query side by e^{+sum} and the key side by
+// e^{-sum}.  Every factor is a gate in (0, 1] or an input: the result is finite for every
+// finite gate.  The adjoint of h0 is dh before token 0.  Reductions over the value
+// columns run inside a warp (shuffles in a fixed pattern), over the state rows through
+// shared memory in a fixed order, so every result is run-to-run deterministic.
 //
 // Window branch: textbook softmax backward in two deterministic kernels, one per
 // query (dq, and the row statistics lse_i and D_i = dyw_i . y_win_i) and one per key
@@ -25,12 +31,18 @@
 namespace lz {
 namespace {
 
-constexpr int kCB = 32;  // chunk of the backward walk
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;  // window kernels
 constexpr int kWarps = kThreads / 32;
 
+constexpr int kSub = 32;  // tokens per checkpoint of the GLA adjoint's forward walk
+
+// Scratch of one GLA adjoint walker (floats): the state at every kSub-th token of its range
+// and the kSub states of the sub-range the reverse walk is in.
+__host__ __device__ inline size_t walk_scratch_floats(int D, int tokens) {
+  return ((size_t)(tokens + kSub - 1) / kSub + kSub) * D * D;
+}
+
 struct BwdWs {
-  float* states;   // [BH][nc][DK][DV] state at the start of each chunk (CUDA-core path)
   unsigned char* gla_tc;  // scratch of the tensor-core GLA path
   float* dvacc;    // [BH][L][DV] GLA part of dv
   float* lse;      // [BH][L]
@@ -39,6 +51,7 @@ struct BwdWs {
   float* p_meta;   // [BH][L][M]
   float* dmeta_part;  // [nsplit][H][M][DK+DV]
   float* mpart;       // per-block meta partials of the tensor-core window path
+  float* walk;        // scratch of the CUDA-core GLA walks (checkpoints and sub-range states)
   int nsplit;
 };
 
@@ -52,12 +65,10 @@ inline int bwd_nsplit(int B, int H, int L) {
   return ns < 1 ? 1 : ns;
 }
 
-// Window scratch and the GLA part of dv first, then the GLA path's own scratch: the
-// chunk states (CUDA cores) or bwd_gla_tc_workspace bytes (tensor cores).
+// Window scratch and the GLA part of dv first, then the tensor-core GLA path's scratch.
 BwdWs carve(unsigned char* p, int B, int H, int L, int dk, int dv, int M, bool tc) {
   BwdWs w;
   const size_t BH = (size_t)B * H;
-  const size_t nc = (L + kCB - 1) / kCB;
   size_t off = 0;
   auto take = [&](size_t floats) {
     float* r = reinterpret_cast<float*>(p + off);
@@ -72,16 +83,13 @@ BwdWs carve(unsigned char* p, int B, int H, int L, int dk, int dv, int M, bool t
   w.nsplit = bwd_nsplit(B, H, L);
   w.dmeta_part = take((size_t)w.nsplit * H * M * (dk + dv));
   w.mpart = dk == 128 && dv == 128 ? take(bwd_win_tc_meta_floats((int)BH, L, M)) : nullptr;
-  w.states = nullptr;
-  w.gla_tc = nullptr;
-  if (tc) w.gla_tc = p + off;
-  else w.states = take(BH * nc * dk * dv);
+  w.gla_tc = tc ? p + off : nullptr;
+  w.walk = tc ? nullptr : take(BH * walk_scratch_floats(dk, L));
   return w;
 }
 
 size_t carve_bytes(int B, int H, int L, int dk, int dv, int M) {
   const size_t BH = (size_t)B * H;
-  const size_t nc = (L + kCB - 1) / kCB;
   size_t off = 0;
   auto take = [&](size_t floats) { off += align_up(floats * sizeof(float) + 1, 256); };
   take(BH * (size_t)L * dv);
@@ -91,254 +99,326 @@ size_t carve_bytes(int B, int H, int L, int dk, int dv, int M) {
   take(BH * (size_t)L * M);
   take((size_t)bwd_nsplit(B, H, L) * H * M * (dk + dv));
   if (dk == 128 && dv == 128) take(bwd_win_tc_meta_floats((int)BH, L, M));
-  const size_t simt = align_up(BH * nc * dk * dv * sizeof(float) + 1, 256);
   const size_t tc = dk == 128 && dv == 128 && L > 0 ? bwd_gla_tc_workspace((int)BH, L) : 0;
-  return off + (simt > tc ? simt : tc);
+  const size_t simt = align_up(BH * walk_scratch_floats(dk, L) * sizeof(float) + 1, 256);
+  return off + (tc > simt ? tc : simt);
 }
 
 // ------------------------------------------------------------------------------------
-// GLA adjoint: one CTA per (b, h), full state in shared memory.
+// GLA adjoint by the recurrence: one CTA of 512 threads per (b, h) (or per wide chunk).
 // ------------------------------------------------------------------------------------
-template <int DK, int DV>
-constexpr size_t gla_bwd_smem_floats() {
-  return 2 * (size_t)DK * (DV + 1)      // G, Hs
-         + 3 * (size_t)kCB * (DK + 1)   // Qt, Kt, Eb
-         + 2 * (size_t)kCB * (DV + 1)   // Vs, dYs
-         + 2 * (size_t)kCB * (kCB + 1)  // A, P
-         + DK;                          // exp(Gamma)
-}
+constexpr int kGThreads = 512;
+constexpr int kGWarps = kGThreads / 32;
+constexpr int kTB = 8;    // tokens staged per step
 
-template <typename T, int DK, int DV>
-__global__ void __launch_bounds__(kThreads) gla_bwd_kernel(BwdArgs a, BwdWs w) {
-  extern __shared__ float sm[];
-  float* G = sm;
-  float* Hs = G + DK * (DV + 1);
-  float* Qt = Hs + DK * (DV + 1);
-  float* Kt = Qt + kCB * (DK + 1);
-  float* Eb = Kt + kCB * (DK + 1);
-  float* Vs = Eb + kCB * (DK + 1);
-  float* dYs = Vs + kCB * (DV + 1);
-  float* A = dYs + kCB * (DV + 1);
-  float* P = A + kCB * (kCB + 1);
-  float* eG = P + kCB * (kCB + 1);
+template <int D>
+struct GbLayout {
+  static constexpr int KPW = D / kGWarps;  // state rows per warp: 8 or 4
+  static constexpr int VPL = D / 32;       // value columns per lane: 4 or 2
+  // floats
+  static constexpr int PQ = 0, PK = PQ + kTB * D, GM = PK + kTB * D, VS = GM + kTB * D,
+                       DY = VS + kTB * D, PV = DY + kTB * D;  // PV: [kTB][kGWarps][D]
+  static constexpr int TOTAL = PV + kTB * kGWarps * D;
+  static_assert(KPW == 4 || KPW == 8, "rows per warp");
+};
 
-  const int bh = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int L = a.L;
-  const int nc = (L + kCB - 1) / kCB;
-  const T* pq = static_cast<const T*>(a.pq) + (size_t)bh * L * DK;
-  const T* pk = static_cast<const T*>(a.pk) + (size_t)bh * L * DK;
-  const T* vg = static_cast<const T*>(a.v) + (size_t)bh * L * DV;
-  const T* dyg = static_cast<const T*>(a.dy) + (size_t)bh * L * DV;
-  const float* lg = a.lg + (size_t)bh * L * DK;
-  T* dpq = static_cast<T*>(a.dpq) + (size_t)bh * L * DK;
-  T* dpk = static_cast<T*>(a.dpk) + (size_t)bh * L * DK;
-  float* dlg = a.dlg + (size_t)bh * L * DK;
-  float* states = w.states + (size_t)bh * nc * DK * DV;
-  float* dvacc = w.dvacc + (size_t)bh * L * DV;
-
-  // Loads chunk ch: cumsum, exp(+-b), features, values (and dy when want_dy).
-  auto load_chunk = [&](int ch, bool want_dy) {
-    const int t0 = ch * kCB;
-    const int n = min(kCB, L - t0);
-    if (tid < DK) {
-      const int kk = tid;
-      float run = 0.f;
-      // eight tokens' loads in flight at a time
-      for (int t8 = 0; t8 < kCB; t8 += 8) {
-        float lv[8], qv[8], kv[8];
+// Sum over the 32 lanes of each of the R values every lane holds (R = 4 or 8), in a fixed
+// butterfly pattern.  Returns, in every lane, the total of row row_of_lane(lane).
+template <int R>
+__device__ __forceinline__ float warp_sum_rows(float (&v)[R]) {
+  const int lane = threadIdx.x & 31;
+  float w[R];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const bool ok = t8 + i < n;
-          const size_t idx = (size_t)(t0 + t8 + i) * DK + kk;
-          lv[i] = ok ? lg[idx] : 0.f;
-          qv[i] = ok ? ld_f(pq + idx) : 0.f;
-          kv[i] = ok ? ld_f(pk + idx) : 0.f;
-        }
+  for (int m = 0; m < R; ++m) w[m] = v[m];
+  int off = 16;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int t = t8 + i;
-          run += lv[i];
-          const float e = t < n ? expf(run) : 1.f;
-          Qt[t * (DK + 1) + kk] = qv[i] * e;
-          Kt[t * (DK + 1) + kk] = t < n ? kv[i] * expf(-run) : 0.f;
-          Eb[t * (DK + 1) + kk] = e;
-        }
-      }
-      eG[kk] = expf(run);
+  for (int n = R; n > 1; n >>= 1, off >>= 1) {
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int m = 0; m < n / 2; ++m) {
+      const float send = up ? w[m] : w[m + n / 2];
+      const float keep = up ? w[m + n / 2] : w[m];
+      w[m] = keep + __shfl_xor_sync(0xffffffffu, send, off);
     }
-    constexpr int kPer = kCB * DV / kThreads;  // elements per thread
-    float vv[kPer], dd[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = tid + i * kThreads;
-      const int t = e / DV, c = e % DV;
+  }
+  float x = w[0];
+  for (; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// The row (0 .. R-1) whose total warp_sum_rows leaves in `lane`; lanes with
+// lane % (32 / R) == 0 hold each row once.
+template <int R>
+__device__ __forceinline__ int row_of_lane(int lane) {
+  return R == 8 ? ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1)
+                : ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+}
+
+// What one pair of walks covers: tokens [t_begin, t_end) of unit bh.
+template <typename T>
+struct GlaWalk {
+  int t_begin, t_end;
+  const T *pq, *pk;          // [BH][L][D] features
+  const float* h_init;       // fp32 [D][D] state before t_begin (null: zeros) ...
+  const bf16* hb_init;       // ... or bf16 [128][128]
+  const bf16* gb_init;       // bf16 [128][128] adjoint after t_end - 1 (null: zeros)
+  float* dh_out;             // fp32 [D][D]: adjoint of the state before t_begin (or null)
+  float* rtot;               // [D]: the range's total of the per-token log-gate term
+                             // phi_q (.) d phi_q - phi_k (.) d phi_k (or null)
+  float* scratch;            // walk_scratch_floats(D, t_end - t_begin) floats
+};
+
+// d log gamma_t = gamma_t <dh_t, h_{t-1}> row by row (the adjoint of h_t against the state
+// before token t): no cancellation between large terms, so the result keeps its relative
+// accuracy however small gamma is.  h_{t-1} comes from a second forward pass over each
+// kSub-token sub-range, started from the checkpoint the first forward walk left and
+// written to scratch; every scratch element is written and read back by the same thread.
+template <typename T, int D>
+__device__ void gla_bwd_walks(const BwdArgs& a, float* sm, int bh, const GlaWalk<T>& g,
+                              float* dvacc) {
+  using Lay = GbLayout<D>;
+  constexpr int KPW = Lay::KPW, VPL = Lay::VPL;
+  constexpr size_t kS = (size_t)D * D;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int L = a.L, k0 = warp * KPW;
+  const int myrow = row_of_lane<KPW>(lane);
+  const bool writer = (lane % (32 / KPW)) == 0;  // holds row myrow's total
+  const int kw = k0 + myrow;
+  const T* pq = g.pq + (size_t)bh * L * D;
+  const T* pk = g.pk + (size_t)bh * L * D;
+  const T* vg = static_cast<const T*>(a.v) + (size_t)bh * L * D;
+  const T* dyg = static_cast<const T*>(a.dy) + (size_t)bh * L * D;
+  const float* lg = a.lg + (size_t)bh * L * D;
+  T* dpq = static_cast<T*>(a.dpq) + (size_t)bh * L * D;
+  T* dpk = static_cast<T*>(a.dpk) + (size_t)bh * L * D;
+  float* dlg = a.dlg + (size_t)bh * L * D;
+  float* dva = dvacc + (size_t)bh * L * D;
+  const int nsub = (g.t_end - g.t_begin + kSub - 1) / kSub;
+  float* ckpt = g.scratch;                    // [nsub][D][D]
+  float* subst = g.scratch + (size_t)nsub * kS;  // [kSub][D][D]
+  // element (i, j) of this thread in a [D][D] state
+  auto eo = [&](int i, int j) { return (size_t)(k0 + i) * D + lane + 32 * j; };
+
+  // tokens [t0, t0 + n) into shared memory (fp32; gamma = exp(log gamma))
+  auto stage = [&](int t0, int n) {
+    for (int e4 = tid; e4 < kTB * D / 4; e4 += kGThreads) {
+      const int t = (4 * e4) / D;
+      const size_t idx = (size_t)(t0 + t) * D + (4 * e4) % D;
       const bool ok = t < n;
-      vv[i] = ok ? ld_f(vg + (size_t)(t0 + t) * DV + c) : 0.f;
-      dd[i] = (ok && want_dy) ? ld_f(dyg + (size_t)(t0 + t) * DV + c) : 0.f;
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(sm + Lay::PQ + 4 * e4) = ok ? ld4(pq + idx) : z;
+      *reinterpret_cast<float4*>(sm + Lay::PK + 4 * e4) = ok ? ld4(pk + idx) : z;
+      *reinterpret_cast<float4*>(sm + Lay::VS + 4 * e4) = ok ? ld4(vg + idx) : z;
+      *reinterpret_cast<float4*>(sm + Lay::DY + 4 * e4) = ok ? ld4(dyg + idx) : z;
+      float4 gm = make_float4(1.f, 1.f, 1.f, 1.f);
+      if (ok) {
+        const float4 l = *reinterpret_cast<const float4*>(lg + idx);
+        gm = make_float4(expf(l.x), expf(l.y), expf(l.z), expf(l.w));
+      }
+      *reinterpret_cast<float4*>(sm + Lay::GM + 4 * e4) = gm;
     }
+  };
+  // h <- diag(gamma_t) h + phi_k_t v_t^T for staged token t
+  auto advance = [&](float (&h)[KPW][VPL], int t) {
+    float vv[VPL];
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = tid + i * kThreads;
-      const int t = e / DV, c = e % DV;
-      Vs[t * (DV + 1) + c] = vv[i];
-      if (want_dy) dYs[t * (DV + 1) + c] = dd[i];
+    for (int j = 0; j < VPL; ++j) vv[j] = sm[Lay::VS + t * D + lane + 32 * j];
+#pragma unroll
+    for (int i = 0; i < KPW; i += 4) {
+      const float4 g4 = *reinterpret_cast<const float4*>(sm + Lay::GM + t * D + k0 + i);
+      const float4 k4 = *reinterpret_cast<const float4*>(sm + Lay::PK + t * D + k0 + i);
+      const float gg[4] = {g4.x, g4.y, g4.z, g4.w}, kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) h[i + u][j] = fmaf(gg[u], h[i + u][j], kk[u] * vv[j]);
     }
   };
 
-  // Forward walk: record the state at the start of every chunk.
-  for (int e = tid; e < DK * DV; e += kThreads) {
-    const int r = e / DV, c = e % DV;
-    Hs[r * (DV + 1) + c] = a.h0 ? a.h0[(size_t)bh * DK * DV + e] : 0.f;
+  float x[KPW][VPL];
+  // ---- forward walk: d phi_q_t = h_t dy_t (and phi_q_t (.) d phi_q_t parked in
+  //      d log gamma_t); the state before every kSub-th token goes to the checkpoints
+#pragma unroll
+  for (int i = 0; i < KPW; ++i)
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+      x[i][j] = g.h_init ? g.h_init[eo(i, j)]
+              : g.hb_init ? __bfloat162float(g.hb_init[(size_t)(k0 + i) * 128 + lane + 32 * j])
+                          : 0.f;
+  for (int t0 = g.t_begin; t0 < g.t_end; t0 += kTB) {
+    const int n = min(kTB, g.t_end - t0);
+    if ((t0 - g.t_begin) % kSub == 0) {
+      float* cp = ckpt + (size_t)((t0 - g.t_begin) / kSub) * kS;
+#pragma unroll
+      for (int i = 0; i < KPW; ++i)
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) cp[eo(i, j)] = x[i][j];
+    }
+    __syncthreads();
+    stage(t0, n);
+    __syncthreads();
+    for (int t = 0; t < n; ++t) {
+      advance(x, t);
+      float dd[VPL], part[KPW];
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) dd[j] = sm[Lay::DY + t * D + lane + 32 * j];
+#pragma unroll
+      for (int i = 0; i < KPW; ++i) {
+        float p = 0.f;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) p = fmaf(x[i][j], dd[j], p);
+        part[i] = p;
+      }
+      const float dq = warp_sum_rows<KPW>(part);
+      if (writer) {
+        const size_t o = (size_t)(t0 + t) * D + kw;
+        dpq[o] = cvt_out<T>(dq);
+        dlg[o] = sm[Lay::PQ + t * D + kw] * dq;
+      }
+    }
   }
-  __syncthreads();
-  for (int ch = 0; ch < nc; ++ch) {
-    {
-      float4* dst = reinterpret_cast<float4*>(states + (size_t)ch * DK * DV);
-      for (int e4 = tid; e4 < DK * DV / 4; e4 += kThreads) {
-        const int e = 4 * e4, r = e / DV, c = e % DV;
-        const float* src = Hs + r * (DV + 1) + c;
-        dst[e4] = make_float4(src[0], src[1], src[2], src[3]);
-      }
-    }
-    load_chunk(ch, false);
-    __syncthreads();
-    for (int e = tid; e < DK * DV; e += kThreads) {
-      const int r = e / DV, c = e % DV;
-      float acc = Hs[r * (DV + 1) + c];
-      for (int s = 0; s < kCB; ++s) acc = fmaf(Kt[s * (DK + 1) + r], Vs[s * (DV + 1) + c], acc);
-      Hs[r * (DV + 1) + c] = eG[r] * acc;
-    }
-    __syncthreads();
-  }
 
-  // Reverse walk.
-  for (int e = tid; e < DK * DV; e += kThreads) G[(e / DV) * (DV + 1) + e % DV] = 0.f;
-  float carry = 0.f;  // running suffix sum of the log-gate term (threads < DK)
-  for (int ch = nc - 1; ch >= 0; --ch) {
-    const int t0 = ch * kCB;
-    const int n = min(kCB, L - t0);
+  // ---- reverse walk, one sub-range of kSub tokens at a time from the last
+#pragma unroll
+  for (int i = 0; i < KPW; ++i)
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+      x[i][j] = g.gb_init ? __bfloat162float(g.gb_init[(size_t)(k0 + i) * 128 + lane + 32 * j]) : 0.f;
+  float rsum = 0.f;  // the range's total of the log-gate term for row kw (writer lanes)
+  for (int sb = nsub - 1; sb >= 0; --sb) {
+    const int c0 = g.t_begin + sb * kSub, cn = min(kSub, g.t_end - c0);
+    // states before each token of the sub-range: subst[u] = h_{c0 + u - 1}
     {
-      // the saved state of this chunk: 16-byte loads, eight in flight per thread
-      const float4* src = reinterpret_cast<const float4*>(states + (size_t)ch * DK * DV);
-      constexpr int kN4 = DK * DV / 4 / kThreads;
+      float h[KPW][VPL];
+      const float* cp = ckpt + (size_t)sb * kS;
 #pragma unroll
-      for (int b8 = 0; b8 < kN4; b8 += 8) {
-        float4 r4[8];
+      for (int i = 0; i < KPW; ++i)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) r4[i] = src[tid + (b8 + i) * kThreads];
+        for (int j = 0; j < VPL; ++j) h[i][j] = cp[eo(i, j)];
+      for (int t0 = c0; t0 < c0 + cn; t0 += kTB) {
+        const int n = min(kTB, c0 + cn - t0);
+        __syncthreads();
+        stage(t0, n);
+        __syncthreads();
+        for (int t = 0; t < n; ++t) {
+          float* st = subst + (size_t)(t0 - c0 + t) * kS;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int e = 4 * (tid + (b8 + i) * kThreads);
-          const int r = e / DV, c = e % DV;
-          float* dst = Hs + r * (DV + 1) + c;
-          dst[0] = r4[i].x;
-          dst[1] = r4[i].y;
-          dst[2] = r4[i].z;
-          dst[3] = r4[i].w;
+          for (int i = 0; i < KPW; ++i)
+#pragma unroll
+            for (int j = 0; j < VPL; ++j) st[eo(i, j)] = h[i][j];
+          if (t0 - c0 + t + 1 < cn) advance(h, t);
         }
       }
     }
-    load_chunk(ch, true);
-    __syncthreads();
-
-    // A = dY V^T, P = Qt Kt^T, both masked to s <= t.
-    for (int e = tid; e < kCB * kCB; e += kThreads) {
-      const int t = e / kCB, s = e % kCB;
-      float x = 0.f, p = 0.f;
-      if (s <= t) {
-        for (int c = 0; c < DV; ++c) x = fmaf(dYs[t * (DV + 1) + c], Vs[s * (DV + 1) + c], x);
-        for (int kk = 0; kk < DK; ++kk) p = fmaf(Qt[t * (DK + 1) + kk], Kt[s * (DK + 1) + kk], p);
-      }
-      A[t * (kCB + 1) + s] = x;
-      P[t * (kCB + 1) + s] = p;
-    }
-    __syncthreads();
-
-    // d_phi_q, d_phi_k, and the per-token log-gate term (stored over Eb).
-    {
-      constexpr int kRowsPerThread = kCB * DK / kThreads;
-      constexpr int kRowStep = kThreads / DK;
-      const int kk = tid % DK;
-      const int r0 = tid / DK;
-      float aq[kRowsPerThread], ak[kRowsPerThread];
-#pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) aq[i] = ak[i] = 0.f;
-      for (int c = 0; c < DV; ++c) {
-        const float hv = Hs[kk * (DV + 1) + c];
-        const float gv = G[kk * (DV + 1) + c];
-#pragma unroll
-        for (int i = 0; i < kRowsPerThread; ++i) {
-          const int t = r0 + kRowStep * i;
-          aq[i] = fmaf(hv, dYs[t * (DV + 1) + c], aq[i]);
-          ak[i] = fmaf(gv, Vs[t * (DV + 1) + c], ak[i]);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) {
-        const int t = r0 + kRowStep * i;
-        float q = aq[i], k = eG[kk] * ak[i];
-        for (int s = 0; s <= t; ++s) q = fmaf(A[t * (kCB + 1) + s], Kt[s * (DK + 1) + kk], q);
-        for (int u = t; u < kCB; ++u) k = fmaf(A[u * (kCB + 1) + t], Qt[u * (DK + 1) + kk], k);
-        const float eb = Eb[t * (DK + 1) + kk];
-        const float dphq = q * eb;
-        const float dphk = k * __frcp_rn(eb);
-        float term = 0.f;
-        if (t < n) {
-          const size_t idx = (size_t)(t0 + t) * DK + kk;
-          dpq[idx] = cvt_out<T>(dphq);
-          dpk[idx] = cvt_out<T>(dphk);
-          term = ld_f(pq + idx) * dphq - ld_f(pk + idx) * dphk;
-        }
-        Eb[t * (DK + 1) + kk] = term;
-      }
-    }
-    __syncthreads();
-    if (tid < DK) {
+    const int nblk = (cn + kTB - 1) / kTB;
+    for (int b = nblk - 1; b >= 0; --b) {
+      const int t0 = c0 + b * kTB;
+      const int n = min(kTB, c0 + cn - t0);
+      __syncthreads();
+      stage(t0, n);
+      __syncthreads();
       for (int t = n - 1; t >= 0; --t) {
-        carry += Eb[t * (DK + 1) + tid];
-        dlg[(size_t)(t0 + t) * DK + tid] = carry;
+        const float* hp = subst + (size_t)(t0 - c0 + t) * kS;  // h_{t-1}
+        float vv[VPL], dd[VPL], part[KPW], pg[KPW], pv[VPL];
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+          vv[j] = sm[Lay::VS + t * D + lane + 32 * j];
+          dd[j] = sm[Lay::DY + t * D + lane + 32 * j];
+          pv[j] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < KPW; i += 4) {
+          const float4 q4 = *reinterpret_cast<const float4*>(sm + Lay::PQ + t * D + k0 + i);
+          const float4 k4 = *reinterpret_cast<const float4*>(sm + Lay::PK + t * D + k0 + i);
+          const float qq[4] = {q4.x, q4.y, q4.z, q4.w}, kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float p = 0.f, q = 0.f;
+#pragma unroll
+            for (int j = 0; j < VPL; ++j) {
+              x[i + u][j] = fmaf(qq[u], dd[j], x[i + u][j]);
+              p = fmaf(x[i + u][j], vv[j], p);
+              q = fmaf(x[i + u][j], hp[eo(i + u, j)], q);
+              pv[j] = fmaf(x[i + u][j], kk[u], pv[j]);
+            }
+            part[i + u] = p;
+            pg[i + u] = q;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) sm[Lay::PV + (t * kGWarps + warp) * D + lane + 32 * j] = pv[j];
+        const float dk = warp_sum_rows<KPW>(part);
+        const float dg = warp_sum_rows<KPW>(pg);
+        if (writer) {
+          const size_t o = (size_t)(t0 + t) * D + kw;
+          dpk[o] = cvt_out<T>(dk);
+          rsum += dlg[o] - sm[Lay::PK + t * D + kw] * dk;
+          dlg[o] = sm[Lay::GM + t * D + kw] * dg;
+        }
+        // move the adjoint to the state before token t
+#pragma unroll
+        for (int i = 0; i < KPW; i += 4) {
+          const float4 g4 = *reinterpret_cast<const float4*>(sm + Lay::GM + t * D + k0 + i);
+          const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int j = 0; j < VPL; ++j) x[i + u][j] *= gg[u];
+        }
+      }
+      __syncthreads();
+      // the GLA part of dv: the warps' partials summed in a fixed order
+      for (int e = tid; e < n * D; e += kGThreads) {
+        const int t = e / D, c = e % D;
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kGWarps; ++w) s += sm[Lay::PV + (t * kGWarps + w) * D + c];
+        dva[(size_t)(t0 + t) * D + c] = s;
       }
     }
+  }
+  if (g.rtot && writer) g.rtot[kw] = rsum;
+  if (g.dh_out) {
+#pragma unroll
+    for (int i = 0; i < KPW; ++i)
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) g.dh_out[eo(i, j)] = x[i][j];
+  }
+}
 
-    // GLA part of dv.
-    {
-      constexpr int kRowsPerThread = kCB * DV / kThreads;
-      constexpr int kRowStep = kThreads / DV;
-      const int c = tid % DV;
-      const int r0 = tid / DV;
-      float acc[kRowsPerThread];
-#pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) acc[i] = 0.f;
-      for (int kk = 0; kk < DK; ++kk) {
-        const float g = eG[kk] * G[kk * (DV + 1) + c];
-#pragma unroll
-        for (int i = 0; i < kRowsPerThread; ++i)
-          acc[i] = fmaf(Kt[(r0 + kRowStep * i) * (DK + 1) + kk], g, acc[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) {
-        const int s = r0 + kRowStep * i;
-        float x = acc[i];
-        for (int t = s; t < kCB; ++t) x = fmaf(P[t * (kCB + 1) + s], dYs[t * (DV + 1) + c], x);
-        if (s < n) dvacc[(size_t)(t0 + s) * DV + c] = x;
-      }
-    }
-    __syncthreads();
+template <typename T, int D>
+__global__ void __launch_bounds__(kGThreads) gla_bwd_kernel(BwdArgs a, float* dvacc, float* scratch) {
+  extern __shared__ float sm[];
+  const int bh = blockIdx.x;
+  GlaWalk<T> g{0, a.L, static_cast<const T*>(a.pq), static_cast<const T*>(a.pk),
+               a.h0 ? a.h0 + (size_t)bh * D * D : nullptr, nullptr, nullptr,
+               a.dh0 ? a.dh0 + (size_t)bh * D * D : nullptr, nullptr,
+               scratch + (size_t)bh * walk_scratch_floats(D, a.L)};
+  gla_bwd_walks<T, D>(a, sm, bh, g, dvacc);
+}
 
-    // Move the state adjoint to the start of this chunk.
-    for (int e = tid; e < DK * DV; e += kThreads) {
-      const int r = e / DV, c = e % DV;
-      float acc = eG[r] * G[r * (DV + 1) + c];
-      for (int t = 0; t < kCB; ++t) acc = fmaf(Qt[t * (DK + 1) + r], dYs[t * (DV + 1) + c], acc);
-      G[r * (DV + 1) + c] = acc;
-    }
+// Wide chunks of the tensor-core backward: one listed chunk per CTA iteration, from the
+// chunk-start state and the unscaled end-of-chunk adjoint the scans left.  d log gamma of
+// the chunk's tokens is final (the suffix pass skips wide chunks); the chunk's total of
+// the log-gate term goes to rtot for the earlier chunks' suffix sums.
+__global__ void __launch_bounds__(kGThreads) bwd_wide_kernel(BwdArgs a, WideFix w, float* dvacc) {
+  extern __shared__ float sm[];
+  pdl_wait();
+  const int total = a.B * a.H * w.nc;  // the list's capacity
+  const int cnt = (int)min(*w.count, (unsigned)total);
+  float* scratch = w.scratch + (size_t)blockIdx.x * walk_scratch_floats(128, kGlaChunk);
+  for (int it = blockIdx.x; it < cnt; it += gridDim.x) {
+    const int chunk = w.list[it];
+    if (chunk < 0 || chunk >= total) continue;
+    const int bh = chunk / w.nc, c = chunk % w.nc;
+    const int tb = c * kGlaChunk, te = min(a.L, tb + kGlaChunk);
+    const size_t so = (size_t)chunk * 128 * 128;
+    GlaWalk<bf16> g{tb, te, w.phq_in, w.phk_in, nullptr, w.hs + so, w.gs + so, nullptr,
+                    w.rtot + (size_t)chunk * 128, scratch};
+    gla_bwd_walks<bf16, 128>(a, sm, bh, g, dvacc);
     __syncthreads();
   }
-  if (a.dh0) {
-    for (int e = tid; e < DK * DV; e += kThreads)
-      a.dh0[(size_t)bh * DK * DV + e] = G[(e / DV) * (DV + 1) + e % DV];
-  }
+  pdl_trigger();
 }
 
 // ------------------------------------------------------------------------------------
@@ -581,13 +661,13 @@ cudaError_t launch_typed(const BwdArgs& a, cudaStream_t s, int* launches) {
   }
   if (tc) {
     if ((e = launch_bwd_gla_tc(a, w.dvacc, w.gla_tc, s, launches)) != cudaSuccess) return e;
-  } else {
-    const size_t smem = gla_bwd_smem_floats<D, D>() * sizeof(float);
-    e = cudaFuncSetAttribute(gla_bwd_kernel<T, D, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  } else if (a.L > 0 || a.dh0) {
+    const size_t smem = GbLayout<D>::TOTAL * sizeof(float);
+    e = cudaFuncSetAttribute(gla_bwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
     trace_begin("gla_bwd_simt", s);
-    gla_bwd_kernel<T, D, D><<<BH, kThreads, smem, s>>>(a, w);
+    gla_bwd_kernel<T, D><<<BH, kGThreads, smem, s>>>(a, w.dvacc, w.walk);
     trace_end(s);
     ++*launches;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -638,8 +718,28 @@ cudaError_t launch_typed(const BwdArgs& a, cudaStream_t s, int* launches) {
 
 }  // namespace
 
+int bwd_wide_ctas(int BH, int nc) { return BH * nc < kWideCtas ? BH * nc : kWideCtas; }
+
+size_t bwd_wide_scratch_bytes(int BH, int nc) {
+  return (size_t)bwd_wide_ctas(BH, nc) * walk_scratch_floats(128, kGlaChunk) * sizeof(float);
+}
+
 size_t bwd_simt_workspace(int B, int H, int L, int dk, int dv, int M) {
   return carve_bytes(B, H, L, dk, dv, M);
+}
+
+cudaError_t launch_bwd_wide_fix(const BwdArgs& a, const WideFix& w, float* dvacc, cudaStream_t s,
+                                int* launches) {
+  const size_t smem = GbLayout<128>::TOTAL * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(bwd_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = bwd_wide_ctas(a.B * a.H, w.nc);
+  trace_begin("bwd_wide_fix", s);
+  e = launch_pdl(bwd_wide_kernel, dim3(grid), dim3(kGThreads), smem, s, a, w, dvacc);
+  trace_end(s);
+  ++*launches;
+  return e;
 }
 
 cudaError_t launch_bwd_simt(const BwdArgs& a, lizard_dtype dt, cudaStream_t s, int* launches) {

@@ -43,6 +43,8 @@ struct GlaWs {
   bf16 *hs, *gs;       // [BH][nc][128][128]
   float* rtot;         // [BH][nc][128]
   float* seg;          // scratch of a split scan, or null
+  int *wide, *wlist;   // wide-chunk flags and list [BH][nc]
+  float* wfix;         // walk scratch of the wide-chunk recomputation
 };
 
 size_t gla_ws_layout(int BH, int L, unsigned char* p, GlaWs* w) {
@@ -64,6 +66,9 @@ size_t gla_ws_layout(int BH, int L, unsigned char* p, GlaWs* w) {
   g.hs = reinterpret_cast<bf16*>(take(st));
   g.gs = reinterpret_cast<bf16*>(take(st));
   g.rtot = reinterpret_cast<float*>(take(vec));
+  g.wide = reinterpret_cast<int*>(take((size_t)BH * nc * sizeof(int)));
+  g.wlist = reinterpret_cast<int*>(take((size_t)BH * nc * sizeof(int)));
+  g.wfix = reinterpret_cast<float*>(take(bwd_wide_scratch_bytes(BH, (int)nc)));
   const size_t seg = gla_seg_scratch(BH, L);
   g.seg = seg ? reinterpret_cast<float*>(take(seg)) : nullptr;
   if (w) *w = g;
@@ -387,10 +392,12 @@ chunk_kernel(const __grid_constant__ ChunkMaps maps, const ChunkP p) {
 // 4. suffix: one CTA per (chunk, b*h), thread = key dimension; adds the sums of the later
 //    chunks to the in-chunk suffix sums.
 // ------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kD) suffix_kernel(int L, int nc, float* dlg, const float* rtot) {
+__global__ void __launch_bounds__(kD) suffix_kernel(int L, int nc, float* dlg, const float* rtot,
+                                                   const int* wide) {
   const int c = blockIdx.x, bh = blockIdx.y, i = threadIdx.x;
   pdl_wait();
-  if (c == nc - 1) {
+  // the last chunk has nothing to add; a wide chunk's values are final already
+  if (c == nc - 1 || wide[(size_t)bh * nc + c]) {
     pdl_trigger();
     return;
   }
@@ -440,6 +447,12 @@ cudaError_t launch_bwd_gla_tc(const BwdArgs& a, float* dvacc, unsigned char* ws,
   // With the forward's context, its Qt, Kt, e^b, Gamma and chunk states are reused and
   // only the adjoint scan runs.
   const bool ctx = a.fwd_ws != nullptr && fwd_ctx_usable(a.dk, a.dv, a.L, a.W, a.M, LIZARD_BF16);
+  // Wide chunks: listed by this call's prep, or by the forward's (count in its header).
+  // From the forward's context their phi_q, phi_k are read where its recomputation left
+  // them (the e^b and Kt sections), otherwise from the inputs.
+  unsigned* wcount = a.status + kWsWideCount;
+  const bf16* phq_in = static_cast<const bf16*>(a.pq);
+  const bf16* phk_in = static_cast<const bf16*>(a.pk);
   if (ctx) {
     const GlaCtx fc = fwd_chunk_tc_ctx(BH, L, a.fwd_ws);
     w.qt = fc.qt;
@@ -447,9 +460,15 @@ cudaError_t launch_bwd_gla_tc(const BwdArgs& a, float* dvacc, unsigned char* ws,
     w.eb = fc.eb;
     w.gam = fc.gam;
     w.hs = fc.hs;
+    w.wide = fc.wide;
+    w.wlist = fc.wlist;
+    wcount = reinterpret_cast<unsigned*>(a.fwd_ws - kWsHeader) + kWsWideCount;
+    phq_in = fc.eb;
+    phk_in = fc.kt;
   }
   GlaStatesArgs ga{BH, L, a.pq, a.pk, a.lg, a.v, a.dy, a.h0, nullptr, a.dh0,
-                   w.qt, w.kt, w.eb, w.gam, w.hs, w.gs, a.status, w.seg};
+                   w.qt, w.kt, w.eb, w.gam, w.hs, w.gs, a.status, w.seg,
+                   w.wide, w.wlist, wcount};
   if (!ctx && (e = launch_gla_prep(ga, s, launches)) != cudaSuccess) return e;
   if ((e = launch_gla_scan(ga, ctx ? GlaScan::kAdjoints : GlaScan::kBoth, s, launches)) != cudaSuccess)
     return e;
@@ -474,9 +493,18 @@ cudaError_t launch_bwd_gla_tc(const BwdArgs& a, float* dvacc, unsigned char* ws,
   ++*launches;
   if (e != cudaSuccess) return e;
 
+  // Wide chunks recomputed exactly (their in-chunk sums and totals of the log-gate term
+  // included) before the suffix pass adds the later chunks' totals.
+  WideFix wf{wcount, w.wlist, nc, w.hs, w.gs};
+  wf.phq_in = phq_in;
+  wf.phk_in = phk_in;
+  wf.rtot = w.rtot;
+  wf.scratch = w.wfix;
+  if ((e = launch_bwd_wide_fix(a, wf, dvacc, s, launches)) != cudaSuccess) return e;
+
   trace_begin("bwd_suffix", s);
   e = launch_pdl(suffix_kernel, dim3(nc, BH), dim3(kD), 0, s, L, nc, a.dlg,
-                 static_cast<const float*>(w.rtot));
+                 static_cast<const float*>(w.rtot), static_cast<const int*>(w.wide));
   trace_end(s);
   ++*launches;
   return e;

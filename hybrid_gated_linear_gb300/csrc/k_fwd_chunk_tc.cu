@@ -421,6 +421,8 @@ size_t fwd_ws_layout(int BH, int L, unsigned char* p, FwdWs* w) {
   g.eb = reinterpret_cast<bf16*>(take((size_t)BH * L * kD * sizeof(bf16)));
   g.gam = reinterpret_cast<float*>(take((size_t)BH * nc * kD * sizeof(float)));
   g.hs = reinterpret_cast<bf16*>(take((size_t)BH * nc * kD * kD * sizeof(bf16)));
+  g.wide = reinterpret_cast<int*>(take((size_t)BH * nc * sizeof(int)));
+  g.wlist = reinterpret_cast<int*>(take((size_t)BH * nc * sizeof(int)));
   const size_t seg = gla_seg_scratch(BH, L);
   g.seg = seg ? reinterpret_cast<float*>(take(seg)) : nullptr;
   if (w) *w = g;
@@ -461,7 +463,8 @@ cudaError_t launch_fwd_chunk_tc(const FwdArgs& a, unsigned char* ws, cudaStream_
   fwd_ws_layout(BH, L, ws, &w);
   cudaError_t e;
   GlaStatesArgs ga{BH, L, a.pq, a.pk, a.lg, a.v, nullptr, a.h0, a.hf, nullptr,
-                   w.qt, w.kt, w.eb, w.gam, w.hs, nullptr, a.status, w.seg};
+                   w.qt, w.kt, w.eb, w.gam, w.hs, nullptr, a.status, w.seg,
+                   w.wide, w.wlist, a.wcount ? a.wcount : a.status + kWsWideCount};
   e = a.xq ? launch_gla_prep_fmap(ga, a.H, a.xq, a.xk, a.wq, a.wk, s, launches)
            : launch_gla_prep(ga, s, launches);
   if (e != cudaSuccess) return e;
@@ -491,7 +494,13 @@ cudaError_t launch_fwd_chunk_tc(const FwdArgs& a, unsigned char* ws, cudaStream_
   FParams p{a.H, L, a.M, a.W, nc, ctas_per_wave(1), a.scale, a.alpha, a.status};
   e = np == 1 ? launch_np<1>(m, p, BH * nc, s) : launch_np<2>(m, p, BH * nc, s);
   ++*launches;
-  return e;
+  if (e != cudaSuccess) return e;
+  // Chunks whose gate range the factorisation cannot hold are recomputed exactly; the
+  // recomputation also leaves their phi_q, phi_k in the context's e^b and Kt sections.
+  WideFix wf{ga.wcount, w.wlist, nc, w.hs};
+  wf.phq = w.eb;
+  wf.phk = w.kt;
+  return launch_fwd_wide_fix(a, wf, s, launches);
 }
 
 }  // namespace lz

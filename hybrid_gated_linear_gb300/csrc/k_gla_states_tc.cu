@@ -5,14 +5,22 @@
 //                       value; Qt = phi_q e^b and Kt = phi_k e^-b in bf16 (and e^b when
 //                       asked), Gamma in fp32 ("Lizard", arXiv 2507.09025, Method:
 //                       parallel form with cumulative gate products, absorbed in log space
-//                       into the features).
+//                       into the features).  e^-b is finite only while |b| stays inside
+//                       the exponent range; a chunk where some |b| exceeds kMaxLogSum is
+//                       "wide": its Kt slot gets the bounded Kh = phi_k e^{Gamma - b}
+//                       instead, and the chunk is flagged and listed for an exact
+//                       recomputation (k_fwd_simt.cu, k_bwd_simt.cu).
 //   scan  (tcgen05)     the state at every chunk start (direction 0)
 //                         h_0 = h0,  h_{c+1} = diag(e^Gamma_c) (h_c + Kt_c^T V_c)
+//                                           = diag(e^Gamma_c) h_c + Kh_c^T V_c   (wide c)
 //                       and, for the backward, the adjoint of the state at every chunk
 //                       end (direction 1)
 //                         G_{nc-1} = 0,  G_{c-1} = diag(e^Gamma_c) G_c + Qt_c^T dY_c
-//                       stored as bf16 h_c and Gt_c = diag(e^Gamma_c) G_c; h_nc is h_final
-//                       and G_{-1} the adjoint of h0 (fp32).  One CTA per (b, h, 32 dv
+//                       stored as bf16 h_c and Gt_c = diag(e^Gamma_c) G_c (G_c itself for a
+//                       wide chunk, whose recomputation needs it unscaled); h_nc is h_final
+//                       and G_{-1} the adjoint of h0 (fp32).  Every operand is bounded by
+//                       the features (b <= 0 for gates in (0, 1]), so the scans stay finite
+//                       for every gate.  One CTA per (b, h, 32 dv
 //                       columns, direction): warp 0 streams the chunks by TMA through a
 //                       ring of 5 (or, two CTAs to an SM, 2) stages, warp 1 issues one
 //                       M=128 N=32 K=128 product per chunk into one TMEM tile per stage,
@@ -76,8 +84,24 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const GlaStatesArgs 
     }
   }
   reinterpret_cast<float2*>(p.gam)[((size_t)bh * nc + c) * (kD / 2) + i2] = make_float2(r0, r1);
-  // e^{+-b} must stay inside the fp32/bf16 range for the factorised form.
-  if (big > kMaxLogSum) raise_status(p.status, kDevCheck);
+  // A wide chunk (e^{-b} out of range for some key dimension): the Kt slot gets the
+  // bounded Kh = phi_k e^{Gamma - b} for the state scan, recomputing b in the same order.
+  const int wide = __syncthreads_or(big > kMaxLogSum);
+  if (wide) {
+    float s0 = 0.f, s1 = 0.f;
+    for (int t = 0; t < n; ++t) {
+      const size_t o = (size_t)t * (kD / 2);
+      const float2 l = lg[o];
+      s0 += l.x;
+      s1 += l.y;
+      const float2 k = __bfloat1622float2(pk[o]);
+      kt[o] = __floats2bfloat162_rn(k.x * expf(r0 - s0), k.y * expf(r1 - s1));
+    }
+  }
+  if (i2 == 0) {
+    p.wide[(size_t)bh * nc + c] = wide;
+    if (wide) p.wlist[atomicAdd(p.wcount, 1u)] = bh * nc + c;
+  }
   pdl_trigger();
 }
 
@@ -247,19 +271,27 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
     // with independent loads into its own column of shared memory (read back by the same
     // thread only), so a global load's latency is paid once per kGamAhead chunks.
     float* gsm = reinterpret_cast<float*>(sm + SC::kGam) + cq * kGamAhead * kD;
+    uint32_t wbits = 0;  // bit v: chunk u + v of the current batch is wide
     for (int u = 0; u < nl && ok; ++u) {
       const int c = dir ? ce - 1 - u : cb + u, s = u % kStages;
       if (u % kGamAhead == 0) {
         const int cnt = min(kGamAhead, nl - u);
         float gv[kGamAhead];
+        int wv[kGamAhead];
 #pragma unroll
         for (int v = 0; v < kGamAhead; ++v) {
           const int cv = dir ? ce - 1 - (u + v) : cb + u + v;
           gv[v] = v < cnt ? p.gam[((size_t)bh * nc + cv) * kD + i] : 0.f;
+          wv[v] = v < cnt ? p.wide[(size_t)bh * nc + cv] : 0;
         }
+        wbits = 0;
 #pragma unroll
-        for (int v = 0; v < kGamAhead; ++v) gsm[v * kD + i] = gv[v];
+        for (int v = 0; v < kGamAhead; ++v) {
+          gsm[v * kD + i] = gv[v];
+          wbits |= (wv[v] != 0 ? 1u : 0u) << v;
+        }
       }
+      const bool wide = (wbits >> (u % kGamAhead)) & 1u;
       const float g = expf(gsm[(u % kGamAhead) * kD + i]);
       if (!(ok = wait_bar(ctl, S_DFULL + s, (u / kStages) & 1))) break;
       tc_fence_after();
@@ -267,7 +299,8 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
       uint32_t d[32];
       tmem_ld32(tl + s * SL, d);
       tmem_ld_wait();
-      if (dir) {
+      // a wide chunk keeps its adjoint unscaled (stored before the decay is applied)
+      if (dir && !wide) {
 #pragma unroll
         for (int k = 0; k < 32; ++k) x[k] *= g;
       }
@@ -276,8 +309,16 @@ scan_kernel(const __grid_constant__ ScanMaps maps, const GlaStatesArgs p, int nc
         dst[k] = make_uint4(pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
                             pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
       if (dir) {
+        if (wide) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) x[k] += __uint_as_float(d[k]);
+          for (int k = 0; k < 32; ++k) x[k] = fmaf(g, x[k], __uint_as_float(d[k]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) x[k] += __uint_as_float(d[k]);
+        }
+      } else if (wide) {  // Kh^T V is already decayed to the chunk end
+#pragma unroll
+        for (int k = 0; k < 32; ++k) x[k] = fmaf(g, x[k], __uint_as_float(d[k]));
       } else {
 #pragma unroll
         for (int k = 0; k < 32; ++k) x[k] = g * (x[k] + __uint_as_float(d[k]));
@@ -385,8 +426,8 @@ cudaError_t launch_gla_scan(const GlaStatesArgs& a, GlaScan which, cudaStream_t 
     e = launch_seg_join(a.BH, nc, nseg, cps, dir, a.gam, a.seg, cap, dir == 0 ? a.h0 : nullptr,
                         dir == 0 ? a.hf : a.dh0, s, launches);
     if (e == cudaSuccess)
-      e = launch_seg_fix(a.BH, nc, nseg, cps, dir, a.gam, a.seg, cap, dir == 0 ? a.hs : a.gs,
-                         dir == 0 && a.h0 != nullptr, s, launches);
+      e = launch_seg_fix(a.BH, nc, nseg, cps, dir, a.gam, a.wide, a.seg, cap,
+                         dir == 0 ? a.hs : a.gs, dir == 0 && a.h0 != nullptr, s, launches);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

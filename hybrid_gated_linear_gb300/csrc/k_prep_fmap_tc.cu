@@ -11,6 +11,9 @@
 //   e^b (bf16), Gamma_c = b at the chunk's last token (fp32)
 // which are exactly the context the unfused prep derives from phi_q, phi_k, so the state
 // scan, the chunk kernel and a later backward run unchanged.  phi itself is never formed.
+// A chunk where some |b| exceeds kMaxLogSum is "wide" (e^{-b} would leave the exponent
+// range): its Kt slot gets the bounded exp(+-x W_k + Gamma - b) for the state scan, and
+// the chunk is flagged and listed for the exact recomputation, as in the unfused prep.
 //
 // Warp 0 issues the TMA loads (x_q, x_k, W_q, W_k and the 128x128 fp32 log-gate tile, all
 // in flight at once) and warms L2 with the tiles of the CTA one wave later; warp 1 issues
@@ -42,7 +45,22 @@ struct PfParams {
   int ahead;    // CTAs per wave: the CTA whose tiles this one prefetches into L2
   float* gam;   // [BH][nc][128]
   unsigned* status;
+  int *wide, *wlist;  // wide-chunk flags and list [BH][nc]
+  unsigned* wcount;
 };
+
+// Named barrier over n threads that also returns whether v was true in any of them.
+__device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
+  __syncwarp();
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
 
 enum { P_LD = 0, P_Z, P_DONE, P_COUNT };
 // x_q, x_k 32 KB each (then the Qt, Kt staging); W_q, W_k 16 KB each (then the e^b
@@ -151,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1) prep_fmap_kernel(const __grid_con
           *reinterpret_cast<float*>(lgs + sw128_offset_f32(r0 + u, j, kT)) = v[u];
       }
     }
-    named_sync(1, 128);
+    const bool wide = named_sync_or(1, 128, big > kMaxLogSum);
     if (ok) ok = wait_bar(ctl, P_Z, 0);
     if (ok) {
       tc_fence_after();
@@ -166,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) prep_fmap_kernel(const __grid_con
         const float sgn = g < 2 ? 1.f : -1.f;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          float bv[16], vq[16], vk[16], ve[16];
+          float bv[16], gv[16], vq[16], vk[16], ve[16];
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             const float4 v = *reinterpret_cast<const float4*>(
@@ -175,12 +193,20 @@ __global__ void __launch_bounds__(kThreads, 1) prep_fmap_kernel(const __grid_con
             bv[4 * m + 1] = v.y;
             bv[4 * m + 2] = v.z;
             bv[4 * m + 3] = v.w;
+            // a wide chunk's keys are referred to the chunk end: Gamma = b of its last token
+            const float4 G = wide ? *reinterpret_cast<const float4*>(
+                                        lgs + sw128_offset_f32(n - 1, 32 * g + 16 * h + 4 * m, kT))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            gv[4 * m] = G.x;
+            gv[4 * m + 1] = G.y;
+            gv[4 * m + 2] = G.z;
+            gv[4 * m + 3] = G.w;
           }
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int i = 16 * h + e;
             vq[e] = __expf(fmaf(sgn, __uint_as_float(zq[i]), bv[e]));
-            vk[e] = __expf(fmaf(sgn, __uint_as_float(zk[i]), -bv[e]));
+            vk[e] = __expf(fmaf(sgn, __uint_as_float(zk[i]), gv[e] - bv[e]));
             ve[e] = __expf(bv[e]);
           }
           // staged over x_q, x_k and the W tiles, which the (completed) MMAs no longer read
@@ -203,8 +229,10 @@ __global__ void __launch_bounds__(kThreads, 1) prep_fmap_kernel(const __grid_con
       bulk_commit();
       bulk_wait_read();
     }
-    // e^{+-b} must stay inside the fp32/bf16 range for the factorised form
-    if (big > kMaxLogSum) raise_status(p.status, kDevCheck);
+    if (threadIdx.x == 64) {
+      p.wide[(size_t)bh * p.nc + c] = wide ? 1 : 0;
+      if (wide) p.wlist[atomicAdd(p.wcount, 1u)] = bh * p.nc + c;
+    }
   }
 
   pdl_trigger();
@@ -234,7 +262,7 @@ cudaError_t launch_gla_prep_fmap(const GlaStatesArgs& a, int H, const void* xq, 
                   make_tma_map_bf16(&m.kt, a.kt, kD, Ll, bhl, 64, kT, sw) &&
                   make_tma_map_bf16(&m.eb, a.eb, kD, Ll, bhl, 64, kT, sw);
   if (!ok) return cudaErrorInvalidValue;
-  const PfParams p{H, a.L, nc, ctas_per_wave(1), a.gam, a.status};
+  const PfParams p{H, a.L, nc, ctas_per_wave(1), a.gam, a.status, a.wide, a.wlist, a.wcount};
   cudaError_t e = cudaFuncSetAttribute(prep_fmap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmem);
   if (e == cudaSuccess)

@@ -10,7 +10,8 @@
 // and every chunk's stored state gets the incoming state carried to it:
 //   h_c  += diag(e^{sum of Gamma over the segment's chunks before c}) H_s
 //   Gt_c += diag(e^{sum of Gamma over chunks c .. segment end}) R_s
-// (Gt_c = diag(e^{Gamma_c}) G_c is what the adjoint scan stores).  All sums run in chunk
+// (Gt_c = diag(e^{Gamma_c}) G_c is what the adjoint scan stores; for a chunk flagged wide it
+// stores G_c itself, and the sum starts at chunk c + 1).  All sums run in chunk
 // order, so the result does not depend on scheduling.
 #include "lizard_dev.cuh"
 #include "lizard_internal.h"
@@ -87,6 +88,7 @@ __global__ void __launch_bounds__(256) seg_join_kernel(int nc, int nseg, int cps
 // row, then the stored bf16 state updated eight elements per thread and step.
 __global__ void __launch_bounds__(256) seg_fix_kernel(int nc, int nseg, int cps, int dir,
                                                       int with_h0, const float* __restrict__ gam,
+                                                      const int* __restrict__ wide,
                                                       const float* __restrict__ segh,
                                                       bf16* __restrict__ st) {
   const int c = blockIdx.x, bh = blockIdx.y, s = c / cps;
@@ -100,7 +102,8 @@ __global__ void __launch_bounds__(256) seg_fix_kernel(int nc, int nseg, int cps,
     // one row per thread: with a CTA per chunk, the many CTAs on an SM hide these sums'
     // load latency (the pass is bound by reading and writing the states)
     const int k = threadIdx.x;
-    const int c0 = dir == 0 ? s * cps : c, c1 = dir == 0 ? c : min(nc, (s + 1) * cps);
+    const int c0 = dir == 0 ? s * cps : c + (wide[(size_t)bh * nc + c] ? 1 : 0);
+    const int c1 = dir == 0 ? c : min(nc, (s + 1) * cps);
     float B = 0.f;
     for (int c2 = c0; c2 < c1; ++c2) B += gam[((size_t)bh * nc + c2) * kD + k];
     f[k] = expf(B);
@@ -163,12 +166,12 @@ cudaError_t launch_seg_join(int BH, int nc, int nseg, int cps, int dir, const fl
 }
 
 cudaError_t launch_seg_fix(int BH, int nc, int nseg, int cps, int dir, const float* gam,
-                           float* seg, int cap, bf16* st, bool with_h0, cudaStream_t s,
-                           int* launches) {
+                           const int* wide, float* seg, int cap, bf16* st, bool with_h0,
+                           cudaStream_t s, int* launches) {
   const float* segh = seg + (size_t)dir * 2 * BH * cap * kS + (size_t)BH * cap * kS;
   trace_begin("scan_fix", s);
   cudaError_t e = launch_pdl(seg_fix_kernel, dim3(nc, BH), dim3(256), 0, s, nc, nseg, cps, dir,
-                             with_h0 ? 1 : 0, gam, segh, st);
+                             with_h0 ? 1 : 0, gam, wide, segh, st);
   trace_end(s);
   ++*launches;
   return e;

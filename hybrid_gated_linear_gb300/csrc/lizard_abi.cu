@@ -679,6 +679,13 @@ lizard_status lizard_attn_fwd_bwd_host(const lizard_dims* dims, const void* phi_
     // compute on `stream` (after this slice's inputs and the copy-out two slices ago)
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, P.ev_in[b], 0);
     if (e == cudaSuccess && si >= 2) e = cudaStreamWaitEvent(s, P.ev_out[b], 0);
+    // every slice lists its own wide chunks: the forward's counter (read back by the
+    // backward from the header slot in front of the forward's scratch) and the
+    // backward's own start from zero
+    unsigned* fwd_wcount = reinterpret_cast<unsigned*>(fwd_ws) + lz::kWsWideCount;
+    if (e == cudaSuccess) e = cudaMemsetAsync(fwd_wcount, 0, sizeof(unsigned), s);
+    if (e == cudaSuccess)
+      e = cudaMemsetAsync(static_cast<unsigned*>(workspace) + lz::kWsWideCount, 0, sizeof(unsigned), s);
     if (e == cudaSuccess) {
       lz::FwdArgs fa{d.B, hs, d.L, d.dk, d.dv, d.M, W_eff, scale, alpha,
                      at(SliceLayout::PQ), at(SliceLayout::PK), at(SliceLayout::V),
@@ -688,6 +695,7 @@ lizard_status lizard_attn_fwd_bwd_host(const lizard_dims* dims, const void* phi_
                      h0 ? static_cast<const float*>(at(SliceLayout::H0)) : nullptr,
                      h_final ? static_cast<float*>(at(SliceLayout::HF)) : nullptr,
                      static_cast<unsigned*>(workspace), fscratch};
+      fa.wcount = fwd_wcount;
       if (d.L > 0 || h_final) e = dispatch_fwd(fa, d.dtype, s, &launches);
     }
     if (e == cudaSuccess) {

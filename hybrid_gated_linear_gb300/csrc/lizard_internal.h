@@ -20,6 +20,8 @@ enum : unsigned { kDevTimeout = 1u, kDevCheck = 2u };
 
 // Every workspace starts with this many bytes: the status word, then zero padding.
 constexpr size_t kWsHeader = 256;
+// Word of the header that counts the tensor-core path's wide chunks (zeroed per call).
+constexpr int kWsWideCount = 4;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -38,6 +40,10 @@ struct FwdArgs {
   // Set instead of pq/pk when the forward starts from the raw projections and the
   // Hedgehog feature map (x [B,H,L,128] bf16, one W [128,64] bf16 per head).
   const void *xq = nullptr, *xk = nullptr, *wq = nullptr, *wk = nullptr;
+  // Counter of the tensor-core path's wide chunks, zero before the call (null: word
+  // kWsWideCount of the status header).  A backward that reuses this forward's context
+  // reads it at word kWsWideCount of the header in front of the forward's scratch.
+  unsigned* wcount = nullptr;
 };
 
 struct BwdArgs {
@@ -137,7 +143,38 @@ struct GlaStatesArgs {
   unsigned* status;
   // gla_seg_scratch bytes for a split scan (null: never split)
   float* seg = nullptr;
+  // Wide chunks (the gate factorisation e^{+b} e^{-b} out of range): flags [BH][nc]
+  // (1 = wide), the list of their indices bh * nc + c, and its length.
+  int* wide = nullptr;
+  int* wlist = nullptr;
+  unsigned* wcount = nullptr;
 };
+
+// The exact recomputation of the wide chunks after the tensor-core kernels: the listed
+// chunks, their chunk-start states hs (and, backward, the unscaled end-of-chunk adjoints
+// gs) [BH][nc][128][128] bf16.  The forward writes the listed chunks' phi_q, phi_k into
+// phq, phk ([BH][L][128] bf16: the context's e^b and Kt sections, which the chunk
+// kernels no longer need for those chunks); a backward from that context reads them
+// back there (phq_in, phk_in), otherwise from its phi_q, phi_k inputs.
+struct WideFix {
+  const unsigned* count;
+  const int* list;
+  int nc;
+  const bf16* hs;
+  const bf16* gs = nullptr;
+  bf16 *phq = nullptr, *phk = nullptr;
+  const bf16 *phq_in = nullptr, *phk_in = nullptr;
+  float* rtot = nullptr;  // backward: per-chunk totals of the log-gate term [BH][nc][128]
+  float* scratch = nullptr;  // backward: bwd_wide_scratch_bytes of walk scratch
+};
+// CTAs of the backward's wide-chunk recomputation (each with its own walk scratch), and
+// the scratch they need.
+constexpr int kWideCtas = 32;
+int bwd_wide_ctas(int BH, int nc);
+size_t bwd_wide_scratch_bytes(int BH, int nc);
+cudaError_t launch_fwd_wide_fix(const FwdArgs& a, const WideFix& w, cudaStream_t s, int* launches);
+cudaError_t launch_bwd_wide_fix(const BwdArgs& a, const WideFix& w, float* dvacc, cudaStream_t s,
+                                int* launches);
 cudaError_t launch_gla_prep(const GlaStatesArgs& a, cudaStream_t s, int* launches);
 // The prep pass fused with the Hedgehog feature map (k_prep_fmap_tc.cu): the same Qt, Kt,
 // e^b and Gamma from x_q, x_k [BH][L][128] and per-head W_q, W_k [H][128][64] (bf16), as
@@ -155,8 +192,8 @@ cudaError_t launch_seg_join(int BH, int nc, int nseg, int cps, int dir, const fl
                             float* seg, int cap, const float* h0, float* fin, cudaStream_t s,
                             int* launches);
 cudaError_t launch_seg_fix(int BH, int nc, int nseg, int cps, int dir, const float* gam,
-                           float* seg, int cap, bf16* st, bool with_h0, cudaStream_t s,
-                           int* launches);
+                           const int* wide, float* seg, int cap, bf16* st, bool with_h0,
+                           cudaStream_t s, int* launches);
 // Which scans: the chunk-start states h_c, the scaled adjoints Gt_c, or both.
 enum class GlaScan { kStates, kAdjoints, kBoth };
 cudaError_t launch_gla_scan(const GlaStatesArgs& a, GlaScan which, cudaStream_t s, int* launches);
@@ -168,6 +205,8 @@ struct GlaCtx {
   float* gam;
   bf16* hs;
   float* seg = nullptr;  // scratch of a split scan (not part of the reused context)
+  int* wide = nullptr;   // wide-chunk flags [BH][nc] and list [BH][nc]
+  int* wlist = nullptr;
 };
 // The context inside a forward workspace (after its header) of B*H units of L tokens.
 GlaCtx fwd_chunk_tc_ctx(int BH, int L, unsigned char* ws);

@@ -91,7 +91,10 @@ size_t lizard_decode_workspace_bytes(const lizard_decode_dims* dims);
  *   h_final [B,H,dk,dv] fp32 final state or NULL.
  * The GLA branch is computed chunkwise with the decay products absorbed in log space
  * into the query/key features ("Lizard", arXiv 2507.09025, Method: hardware-aware
- * reparameterisation); the result equals the recurrence up to rounding.
+ * reparameterisation); the result equals the recurrence up to rounding.  Every finite
+ * log_gamma <= 0 gives a finite result: a 128-token chunk whose cumulative log gate
+ * leaves [-80, 80] (where e^{-b} would overflow) is recomputed exactly by the recurrence
+ * on CUDA cores, so strong gates cost time, not accuracy.
  */
 lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* phi_q, const void* phi_k,
                               const void* v, const float* log_gamma, const void* q,
@@ -116,8 +119,9 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* phi_q, const 
  *   lizard_fwd_workspace_bytes(dims, W); it holds the same saved context as
  *   lizard_attn_fwd's, so lizard_attn_bwd(..., phi_q = NULL, phi_k = NULL, ...,
  *   fwd_workspace = this workspace) returns d_phi_q, d_phi_k, from which
- *   lizard_feature_map_bwd gives the gradients of x_q, x_k, W_q, W_k.  A chunk-local
- *   log-gate sum beyond +-80 sets LIZARD_ERR_DEVICE_CHECK, as in lizard_attn_fwd.
+ *   lizard_feature_map_bwd gives the gradients of x_q, x_k, W_q, W_k.  Chunks whose
+ *   log-gate range is too wide for the factorised form are recomputed exactly, as in
+ *   lizard_attn_fwd (their phi is formed there in fp32 from x and W).
  */
 lizard_status lizard_attn_fwd_fmap(const lizard_dims* dims, const void* x_q, const void* x_k,
                                    const void* w_q, const void* w_k, const void* v,

@@ -104,6 +104,29 @@ def make_fwd_inputs(B, H, L, dk, dv, M, dtype="bf16", gate="plain", seed=0, with
     return out
 
 
+STRONG_GATES = ("const1", "const3", "const20", "bimodal5", "mixed")
+
+
+def strong_log_gate(kind: str, B, H, L, dk, seed=0) -> np.ndarray:
+    """Gates far stronger than the workloads' logsigmoid(g)/16, [B,H,L,dk] float32:
+    const1 / const3 / const20: log gamma = -1, -3, -20 for every token and key dimension;
+    bimodal5: the first half of the key dimensions -5 per token, the second half
+    logsigmoid(g + 4)/16; mixed: logsigmoid(g)/16 for tokens before L/3, then -1."""
+    if kind.startswith("const"):
+        return np.full((B, H, L, dk), -float(kind[5:]), dtype=np.float32)
+    rng = np.random.default_rng(seed)
+    g = rng.standard_normal((B, H, L, dk))
+    if kind == "bimodal5":
+        out = log_gate(g, np.full(dk, 4.0))
+        out[..., : dk // 2] = -5.0
+        return out
+    if kind == "mixed":
+        out = log_gate(g, np.zeros(dk))
+        out[:, :, L // 3:, :] = -1.0
+        return out
+    raise ValueError(f"unknown gate {kind!r}")
+
+
 def make_fmap_inputs(B, H, L, D, F, dtype="bf16", seed=0, with_dphi=False):
     """Inputs of a feature-map call: x [B,H,L,D] ~ N(0,1) and per-head W [H,D,F] ~
     N(0, 1/D) (so that x W is about unit variance), each rounded to the storage dtype;

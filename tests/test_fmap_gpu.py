@@ -230,14 +230,6 @@ def test_fused_training_step_gradients_match_oracle(L, W):
     assert max(errs.values()) <= TOL["bf16"], errs
 
 
-def test_fused_forward_flags_gate_sums_out_of_range():
-    import hybrid_gated_linear_gb300 as lz
-    x = _fused_inputs(1, 1, 256, 4, seed=730)
-    x["log_gamma"] = np.full_like(x["log_gamma"], -2.0)  # chunk sums reach -256
-    _, _, ws, _, _ = _run_fused(x, 64, 1.0, want_hf=False)
-    assert lz.lizard_check_device_errors(ws) == 5  # LIZARD_ERR_DEVICE_CHECK
-
-
 def test_fused_forward_without_tokens_carries_h0():
     import torch
     import hybrid_gated_linear_gb300 as lz
