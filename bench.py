@@ -5,10 +5,13 @@ workload (B=1, H=32, L=4096, d=128, W=64, M=4, bf16 tensors, fp32 log-gate/state
 ``value`` is tokens/s of the whole job (B*L tokens per step per GPU, all heads); every
 rank runs its own independent batch (weak scaling, no collective on the data path).
 
-Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the launch
-stream with an L2 flush (a 256 MiB write) between steps, outside the events; inputs are
-also larger than L2.  A barrier and a device synchronise bracket the timed region and
-the slowest rank's time is reported.  ``e2e`` repeats the step through the same public
+Timing: W warm-up steps, then three blocks of K steps, each step bracketed by CUDA
+events on the launch stream with an L2 flush (a 256 MiB write) between steps, outside
+the events; inputs are also larger than L2.  A barrier and a device synchronise bracket
+every block; the median of the three block means is reported (the slowest rank's), with
+the clock samples of each block.  ``roofline`` is the whole step against the operator's
+algorithmic bytes (2048 B per (token, head) forward + 3840 B backward); the dominant
+kernel's figures are reported beside it.  ``e2e`` repeats the step through the same public
 calls with pinned host buffers, copying inputs in and every output back each step.
 ``--impl reference`` times the fp64 oracle on the host cores on a bounded sample of the
 same workload and prints the same kind of line.
@@ -25,6 +28,8 @@ import sys
 import tempfile
 import threading
 import time
+
+import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -56,11 +61,10 @@ ALGO_BYTES_PER_TOKEN_HEAD = {
     "fmap_bwd_tc": 3 * 256,                   # x, d_phi -> d_x
     "fwd_prep_fmap": 2 * 256 + 512 + 3 * 256,  # x_q, x_k, log_gamma -> Qt, Kt, e^b
 }
-# DRAM bytes (read + write) per (token, head) from the ncu captures summarised under
-# profiles/, each with the sha256 of the kernel source it was taken on: a kernel whose
-# source changed since then reports "traffic": null.
+# DRAM bytes (read + write) per (token, head) from the ncu capture of the step's kernels
+# (its summary is kept under profiles/), each with the sha256 of the kernel source it was
+# taken on: a kernel whose source changed since then reports "traffic": null.
 PROFILED_TRAFFIC = {
-    # profiles/ncu_step_kernels_llama3_8b.md
     "fwd_prep": {"bytes_per_token_head": 1455, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
                "sha256": "2c9e1070d71be0a0efe6535b2264d9e75664ab6847f4766b7ca3fc3b780ccd0c"},
     "fwd_scan_tc": {"bytes_per_token_head": 541, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
@@ -107,6 +111,7 @@ class ClockSampler:
         self.proc = None
         self.path = None
         self.t0 = self.t1 = None
+        self.windows = []  # (start, end) of every timed block
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -131,6 +136,7 @@ class ClockSampler:
 
     def mark_end(self):
         self.t1 = time.time()
+        self.windows.append((self.t0, self.t1))
         time.sleep(2 * self.INTERVAL_MS / 1000.0)
 
     def __exit__(self, *exc):
@@ -166,18 +172,26 @@ class ClockSampler:
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         slack = self.INTERVAL_MS / 1000.0
-        inside = [r for r in rows
-                  if self.t0 is not None and self._when(r[0]) is not None
-                  and self.t0 - slack <= self._when(r[0]) <= self.t1 + slack]
-        use = inside if inside else rows
-        sm = [float(r[2]) for r in use if r[2].replace(".", "").isdigit()]
-        mx = [float(r[3]) for r in use if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in use for i in range(4) if r[6 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(inside), "interval_ms": self.INTERVAL_MS,
-                "window": "timed region" if inside else "whole timing block (none inside)"}
+
+        def stats(use):
+            sm = [float(r[2]) for r in use if r[2].replace(".", "").isdigit()]
+            mx = [float(r[3]) for r in use if r[3].replace(".", "").isdigit()]
+            reasons = sorted({names[i] for r in use for i in range(4) if r[6 + i].lower() == "active"})
+            return {"sm_mhz": statistics.median(sm) if sm else None,
+                    "sm_max_mhz": max(mx) if mx else None, "reasons": reasons}
+
+        blocks, inside = [], []
+        for (a, b) in self.windows:
+            rs = [r for r in rows if self._when(r[0]) is not None
+                  and a - slack <= self._when(r[0]) <= b + slack]
+            inside += rs
+            blocks.append(dict(stats(rs), samples=len(rs)))
+        out = stats(inside if inside else rows)
+        out.update({"samples": len(inside), "interval_ms": self.INTERVAL_MS,
+                    "window": "timed blocks" if inside else "whole timing block (none inside)",
+                    "blocks": blocks})
+        return out
 
 
 def _dist():
@@ -344,8 +358,34 @@ def _profiled_traffic(kernel, units):
     return rec["bytes_per_token_head"] * units
 
 
+STEP_BYTES_PER_TOKEN_HEAD = 2048 + 3840  # the operator's forward + backward
+BLOCKS = 3  # timed blocks of K steps; the median block is reported
+
+
+def _step_roofline(ms, w, peaks, dominant):
+    """The whole fwd+bwd step against the operator's algorithmic bytes per (token, head):
+    forward 2048 (phi_q, phi_k, v, q, k in bf16, log gamma fp32, y bf16), backward 3840
+    (those inputs and dy; five bf16 gradients and d log gamma fp32)."""
+    units = w["B"] * w["H"] * w["L"]
+    nbytes = STEP_BYTES_PER_TOKEN_HEAD * units
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    traffic = None
+    if dominant is not None:
+        parts = [_profiled_traffic(k, units) for k in PROFILED_TRAFFIC]
+        traffic = sum(parts) if all(p is not None for p in parts) else None
+    return {"kernel": "fwd+bwd step (every kernel of lizard_attn_fwd and lizard_attn_bwd)",
+            "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+            "algorithmic_bytes_per_step": nbytes,
+            "algorithmic_bytes_per_token_head": STEP_BYTES_PER_TOKEN_HEAD,
+            "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
+            "traffic_note": "ncu dram bytes summed over the step's profiled kernels, per step; "
+                            "null when any of their sources changed since the capture"}
+
+
 def _roofline_from_trace(trace, w, peaks, steps):
-    """Dominant kernel over the timed steps -> roofline object."""
+    """Dominant kernel over the traced steps -> its roofline object (against the bytes the
+    kernel must move in this design) and every kernel's time, share and fraction."""
     tot, cnt = {}, {}
     for name, ms in trace:
         tot[name] = tot.get(name, 0.0) + ms
@@ -513,19 +553,23 @@ def _fmap_part(dev, peaks, flush, prob, reps=20):
     return out
 
 
-def _long_context_part(dev, peaks, flush, reps=5):
-    """Long-context forward with few (batch, head) units: B=1, H=4, L=65536, W=128, M=8
-    (the 64K shape with 4 heads), where the state scan is split into segments.  Forward
-    timed with CUDA events (L2 flushed before each call), then one traced call for the
-    per-kernel times."""
+def _long_context_inputs():
+    import synth
+    return synth.workload_inputs("long_ctx_64k")
+
+
+def _long_context_part(dev, peaks, flush, x, H=32, reps=5):
+    """Long-context forward B=1, L=65536, W=128, M=8 with the bimodal gate: with H = 32 the
+    long-context workload itself; with H = 4 (its first four heads) few (batch, head)
+    units, where the state scan is split into segments.  Forward timed with CUDA events
+    (L2 flushed before each call), then one traced call for the per-kernel times."""
     import torch
 
     import hybrid_gated_linear_gb300 as lz
-    import synth
-    B, H, L, d, W, M = 1, 4, 65536, 128, 128, 8
-    x = synth.make_fwd_inputs(B, H, L, d, d, M, "bf16", "bimodal", seed=1007)
+    B, L, d, W, M = 1, 65536, 128, 128, 8
+    x = {n: (a[:H] if n in ("meta_k", "meta_v") else a[:, :H]) for n, a in x.items()}
     bf = torch.bfloat16
-    t = {n: torch.from_numpy(a).to(dev) for n, a in x.items()}
+    t = {n: torch.from_numpy(np.ascontiguousarray(a)).to(dev) for n, a in x.items()}
     for n in t:
         if n != "log_gamma":
             t[n] = t[n].to(bf)
@@ -556,12 +600,41 @@ def _long_context_part(dev, peaks, flush, reps=5):
     ms = statistics.mean(times)
     units = B * H * L
     gbs = 2048 * units / (ms * 1e-3) / 1e9
-    return {"workload": f"long-context forward B={B}, H={H}, L={L}, d={d}, W={W}, M={M}, bf16 "
-                        "(state scan split into segments)",
+    return {"workload": f"long-context forward B={B}, H={H}, L={L}, d={d}, W={W}, M={M}, bf16, "
+                        "bimodal gate" + (" (state scan split into segments)" if H < 32 else ""),
             "ms": ms, "tokens_per_s": B * L / (ms * 1e-3), "launches": launches,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": 2048 * units},
             "kernels_ms": {name: round(v, 4) for name, v in trace}}
+
+
+def _train_part(dev, peaks, flush, steps):
+    """The training workload's fwd+bwd step (B=8, H=32, L=2048, d=128, W=64, M=4, slow
+    gate), timed like the headline step: mean over `steps` steps with the L2 flushed
+    before each."""
+    import torch
+
+    import synth
+    w = synth.WORKLOADS["train_fwd_bwd"]
+    x = synth.workload_inputs("train_fwd_bwd")
+    prob = Problem(x, w, dev)
+    del x
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        prob.step()
+    times = _time_steps(prob.step, steps, flush, stream)
+    if prob.lz.lizard_check_device_errors(prob.ws_b) != 0:
+        raise RuntimeError("training step: device status word set")
+    ms = statistics.mean(times)
+    units = w["B"] * w["H"] * w["L"]
+    nbytes = STEP_BYTES_PER_TOKEN_HEAD * units
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"training fwd+bwd B={w['B']}, H={w['H']}, L={w['L']}, d={w['dk']}, "
+                        f"W={w['W']}, M={w['M']}, bf16, slow gate", "ms": ms,
+            "tokens_per_s": w["B"] * w["L"] / (ms * 1e-3), "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "algorithmic_bytes": nbytes}}
 
 
 def _e2e(prob, steps, dev):
@@ -655,15 +728,18 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     with ClockSampler(local) as clk:
-        _barrier(world)
-        torch.cuda.synchronize()
-        prob.launches = 0
-        clk.mark_start()
-        times = _time_steps(prob.step, args.steps, flush, stream)
-        clk.mark_end()
-        torch.cuda.synchronize()
-        _barrier(world)
-        launches = prob.launches
+        block_ms, launches = [], 0
+        for _ in range(BLOCKS):
+            _barrier(world)
+            torch.cuda.synchronize()
+            prob.launches = 0
+            clk.mark_start()
+            times = _time_steps(prob.step, args.steps, flush, stream)
+            clk.mark_end()
+            torch.cuda.synchronize()
+            _barrier(world)
+            launches = prob.launches
+            block_ms.append(statistics.mean(times))
         # Per-kernel durations: the same K steps again with a CUDA event pair around every
         # kernel (events between kernels stop consecutive kernels from overlapping, so this
         # pass is not the one `value` is taken from).
@@ -676,11 +752,12 @@ def run_ours(args):
         bwd_times = _time_steps(prob.bwd, args.steps, flush, stream)
     clocks = clk.summary()
 
-    ms = statistics.mean(times)
+    ms = statistics.median(block_ms)
     ms = _max_over_ranks(ms, world, dev)
     tokens = w["B"] * w["L"]
     value = world * tokens / (ms * 1e-3)
-    roof, kernels = _roofline_from_trace(trace, w, peaks, args.steps)
+    dom, kernels = _roofline_from_trace(trace, w, peaks, args.steps)
+    roof = _step_roofline(ms, w, peaks, dom)
     fwd_ms = statistics.mean(fwd_times)
     bwd_ms = statistics.mean(bwd_times)
     units = w["B"] * w["H"] * w["L"]
@@ -694,6 +771,8 @@ def run_ours(args):
                 "roofline_frac": bwd_bytes / (bwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                 "algorithmic_bytes": bwd_bytes},
         "kernels": kernels,
+        "dominant_kernel": dom,
+        "block_ms": block_ms,
         "traced_ms_per_step": statistics.mean(traced),
         "kernel_timing": "CUDA events around every kernel in a second pass of the same K steps "
                          "right after the timed region (the event pairs keep consecutive "
@@ -708,9 +787,20 @@ def run_ours(args):
     except Exception as e:  # reported, never hidden
         parts["feature_map"] = {"error": repr(e)}
     try:
-        parts["long_context"] = _long_context_part(dev, peaks, flush)
+        xl = _long_context_inputs()
+        for key, H in (("long_context", 32), ("long_context_split", 4)):
+            try:
+                parts[key] = _long_context_part(dev, peaks, flush, xl, H=H)
+            except Exception as e:  # reported, never hidden
+                parts[key] = {"error": repr(e)}
+        del xl
     except Exception as e:  # reported, never hidden
         parts["long_context"] = {"error": repr(e)}
+    if not args.no_train_part:
+        try:
+            parts["train_step"] = _train_part(dev, peaks, flush, args.steps)
+        except Exception as e:  # reported, never hidden
+            parts["train_step"] = {"error": repr(e)}
     e2e_ms, h2d, d2h = _e2e(prob, max(3, args.steps // 2), dev)
     e2e_ms = _max_over_ranks(e2e_ms, world, dev)
 
@@ -719,7 +809,8 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Gaussian inputs, random meta tokens)",
-        "config": _config(w), "roofline": roof, "gpu_launches": launches, "clocks": clocks,
+        "config": _config(w), "roofline": roof, "gpu_launches": launches,
+        "timed_blocks": BLOCKS, "clocks": clocks,
         "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "parts": parts,
@@ -738,6 +829,18 @@ def run_ours(args):
     return 0
 
 
+def _relaunch(args_list, n):
+    """Runs this script again as n ranks on this node (one process per GPU)."""
+    import socket
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__)] + args_list
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -745,9 +848,21 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-train-part", action="store_true",
+                    help="skip the training-workload line in parts (a shorter run)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    world = int(os.environ.get("WORLD_SIZE", "0"))
+    if world == 0 and args.gpus > 1:
+        # not started under torchrun: start the N ranks here
+        return _relaunch(sys.argv[1:], args.gpus)
+    if max(world, 1) != args.gpus:
+        sys.stderr.write(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; run N ranks "
+                         "with torchrun --nproc-per-node N, or without torchrun\n")
+        return 2
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -26,7 +26,8 @@ __all__ = [
     "lizard_attn_fwd_bwd_host", "lizard_fwd_bwd_host_workspace_bytes",
     "lizard_decode_ring_fill", "lizard_state_combine", "lizard_fmap_dims",
     "lizard_feature_map_fwd", "lizard_feature_map_bwd", "lizard_feature_map_workspace_bytes",
-    "lizard_attn_fwd_fmap", "LIZARD_F32", "LIZARD_BF16", "EXPORTED_SYMBOLS",
+    "lizard_attn_fwd_fmap", "lizard_selftest_wait_timeout", "LIZARD_F32", "LIZARD_BF16",
+    "EXPORTED_SYMBOLS",
 ]
 
 LIZARD_F32 = 0
@@ -41,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "lizard_decode_step_noalloc", "lizard_attn_fwd_bwd_host", "lizard_fwd_bwd_host_workspace_bytes",
     "lizard_decode_ring_fill", "lizard_state_combine", "lizard_feature_map_fwd",
     "lizard_feature_map_bwd", "lizard_feature_map_workspace_bytes", "lizard_attn_fwd_fmap",
+    "lizard_selftest_wait_timeout",
 )
 
 STATUS_NAMES = {0: "LIZARD_OK", 1: "LIZARD_ERR_INVALID_ARG", 2: "LIZARD_ERR_UNSUPPORTED",
@@ -117,6 +119,7 @@ def library():
                 "lizard_feature_map_fwd": (I32, [FMP, P, P, P, P, SZ, P]),
                 "lizard_feature_map_bwd": (I32, [FMP, P, P, P, P, P, P, SZ, P]),
                 "lizard_attn_fwd_bwd_host": (I32, [DP] + [P] * 8 + [I32, F] + [P] * 13 + [P, SZ, P]),
+                "lizard_selftest_wait_timeout": (I32, [P, SZ, ctypes.c_int64, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -202,6 +205,13 @@ def lizard_workspace_init(workspace, stream=None):
 def lizard_check_device_errors(workspace, stream=None) -> int:
     """Synchronises the stream and returns the device status (0 = OK); does not raise."""
     return library().lizard_check_device_errors(_ptr(workspace), _stream(stream))
+
+
+def lizard_selftest_wait_timeout(workspace, wait_cycles: int, stream=None):
+    """Makes one bounded device wait run out on purpose (see include/lizard.h)."""
+    _check(library().lizard_selftest_wait_timeout(_ptr(workspace), _ws_bytes(workspace),
+                                                  int(wait_cycles), _stream(stream)),
+           "lizard_selftest_wait_timeout")
 
 
 def _ws_bytes(ws):

@@ -168,6 +168,8 @@ cudaError_t copy_heads(void* dst, const void* src, const lizard_dims& d, int h0,
 
 }  // namespace
 
+void lz::set_last_launches(int n) { g_last_launches = n; }
+
 extern "C" {
 
 int32_t lizard_abi_version(void) { return LIZARD_ABI_VERSION; }

@@ -78,6 +78,9 @@ struct DecArgs {
   unsigned* status;
 };
 
+// The value lizard_last_launch_count returns on this host thread (set by every entry point).
+void set_last_launches(int n);
+
 // Optional per-kernel event tracing (no-ops unless enabled on this host thread).
 void trace_begin(const char* name, cudaStream_t s);
 void trace_end(cudaStream_t s);

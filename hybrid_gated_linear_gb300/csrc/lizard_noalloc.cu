@@ -58,6 +58,7 @@ extern "C" lizard_status lizard_decode_step_noalloc(
     const float* log_gamma, const void* q, const void* k, const void* meta_k,
     const void* meta_v, int32_t W, float alpha, float* h, void* k_ring, void* v_ring,
     int64_t* pos, void* y, void* stream) {
+  lz::set_last_launches(0);
   if (!dims) return LIZARD_ERR_INVALID_ARG;
   const lizard_decode_dims& d = *dims;
   if (d.N < 1 || d.H < 1 || d.M < 0 || d.M > 16 || W < 1 || W > 1024 || !isfinite(alpha) ||
@@ -101,5 +102,7 @@ extern "C" lizard_status lizard_decode_step_noalloc(
                 y, reinterpret_cast<unsigned*>(base + lz::kWsHeader),
                 reinterpret_cast<unsigned*>(base)};
   int launches = 0;
-  return lz::launch_decode(a, d.dtype, s, &launches) == cudaSuccess ? LIZARD_OK : LIZARD_ERR_CUDA;
+  const cudaError_t e = lz::launch_decode(a, d.dtype, s, &launches);
+  lz::set_last_launches(launches);
+  return e == cudaSuccess ? LIZARD_OK : LIZARD_ERR_CUDA;
 }

@@ -18,10 +18,11 @@ struct Ctl {
   int abort;
 };
 
-// Bounded wait: gives up (and raises the CTA's abort flag) after kWaitCycles SM clock
-// cycles, or as soon as another role has aborted.
+// Bounded wait: gives up (and raises the CTA's abort flag) after `limit` SM clock cycles
+// (kWaitCycles unless a self-test asks for less), or as soon as another role has aborted.
 template <int NB>
-__device__ __forceinline__ bool wait_bar(Ctl<NB>* ctl, int i, uint32_t parity) {
+__device__ __forceinline__ bool wait_bar(Ctl<NB>* ctl, int i, uint32_t parity,
+                                         long long limit = kWaitCycles) {
   uint64_t* b = &ctl->bar[i];
   if (mbar_try_wait(b, parity)) return true;
   const long long t0 = clock64();
@@ -30,7 +31,7 @@ __device__ __forceinline__ bool wait_bar(Ctl<NB>* ctl, int i, uint32_t parity) {
     for (int k = 0; k < 32; ++k)
       if (mbar_try_wait(b, parity)) return true;
     if (*(volatile int*)&ctl->abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       *(volatile int*)&ctl->abort = 1;
       return false;
     }

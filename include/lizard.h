@@ -222,8 +222,9 @@ lizard_status lizard_decode_step(const lizard_decode_dims* dims, const void* phi
  * current device; make that first call before any stream capture begins.  Each call
  * clears the counters on `stream` before its kernel.  Every call in the process shares
  * the one array, so calls whose work overlaps on the GPU (other streams, other threads)
- * race on it: order them.  These calls report no device status word and are not counted
- * by lizard_last_launch_count.  Nothing is allocated or freed.
+ * race on it: order them.  These calls report no device status word; their kernels are
+ * counted by lizard_last_launch_count like every other call's.  Nothing is allocated or
+ * freed.
  */
 #define LIZARD_NOALLOC_MAX_SEQUENCES 16384
 lizard_status lizard_decode_step_noalloc(const lizard_decode_dims* dims, const void* phi_q,
@@ -317,6 +318,21 @@ lizard_status lizard_workspace_init(void* workspace, size_t workspace_bytes, voi
  * the stream itself reports an error).
  */
 lizard_status lizard_check_device_errors(void* workspace, void* stream);
+
+/*
+ * Self-test of the device-side failure detection (a library service; the pages have no
+ * counterpart).  Every wait of the tile kernels on an mbarrier is bounded: when it runs
+ * out the CTA stops its other roles, drains what it has in flight, frees its tensor
+ * memory, returns, and the call's workspace status word reads LIZARD_ERR_TIMEOUT.  No
+ * valid input makes a wait run out, so this call makes one run out on purpose: a single
+ * CTA arms a barrier for bytes that no copy will deliver (nothing is in flight, so
+ * nothing can fault) and waits wait_cycles SM clock cycles (1 .. about 2e9; 2e5 is about
+ * 100 us).  Afterwards lizard_check_device_errors(workspace) returns LIZARD_ERR_TIMEOUT
+ * and clears the word, and the context stays usable.  workspace: at least 256 bytes,
+ * 16-byte aligned; its status word is zeroed first on `stream`.
+ */
+lizard_status lizard_selftest_wait_timeout(void* workspace, size_t workspace_bytes,
+                                           int64_t wait_cycles, void* stream);
 
 /* Static description of a status code. */
 const char* lizard_status_string(lizard_status status);
