@@ -26,8 +26,9 @@ __all__ = [
     "lizard_attn_fwd_bwd_host", "lizard_fwd_bwd_host_workspace_bytes",
     "lizard_decode_ring_fill", "lizard_state_combine", "lizard_fmap_dims",
     "lizard_feature_map_fwd", "lizard_feature_map_bwd", "lizard_feature_map_workspace_bytes",
-    "lizard_attn_fwd_fmap", "lizard_selftest_wait_timeout", "LIZARD_F32", "LIZARD_BF16",
-    "EXPORTED_SYMBOLS",
+    "lizard_attn_fwd_fmap", "lizard_selftest_wait_timeout", "lizard_gate_dims",
+    "lizard_gate_fwd", "lizard_gate_bwd", "lizard_gate_workspace_bytes", "LIZARD_F32",
+    "LIZARD_BF16", "EXPORTED_SYMBOLS",
 ]
 
 LIZARD_F32 = 0
@@ -42,7 +43,8 @@ EXPORTED_SYMBOLS = (
     "lizard_decode_step_noalloc", "lizard_attn_fwd_bwd_host", "lizard_fwd_bwd_host_workspace_bytes",
     "lizard_decode_ring_fill", "lizard_state_combine", "lizard_feature_map_fwd",
     "lizard_feature_map_bwd", "lizard_feature_map_workspace_bytes", "lizard_attn_fwd_fmap",
-    "lizard_selftest_wait_timeout",
+    "lizard_selftest_wait_timeout", "lizard_gate_fwd", "lizard_gate_bwd",
+    "lizard_gate_workspace_bytes",
 )
 
 STATUS_NAMES = {0: "LIZARD_OK", 1: "LIZARD_ERR_INVALID_ARG", 2: "LIZARD_ERR_UNSUPPORTED",
@@ -67,6 +69,12 @@ class lizard_decode_dims(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int32), ("H", ctypes.c_int32), ("dk", ctypes.c_int32),
                 ("dv", ctypes.c_int32), ("M", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("scale", ctypes.c_float)]
+
+
+class lizard_gate_dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("L", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("dk", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("tau", ctypes.c_float)]
 
 
 class lizard_fmap_dims(ctypes.Structure):
@@ -95,6 +103,7 @@ def library():
             P, I32, F, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
             DP, DDP = ctypes.POINTER(lizard_dims), ctypes.POINTER(lizard_decode_dims)
             FMP = ctypes.POINTER(lizard_fmap_dims)
+            GDP = ctypes.POINTER(lizard_gate_dims)
             sig = {
                 "lizard_attn_fwd": (I32, [DP] + [P] * 8 + [I32, F, P, P, P, P, SZ, P]),
                 "lizard_attn_bwd": (I32, [DP] + [P] * 8 + [I32, F] + [P] * 12 + [P, SZ, P]),
@@ -120,6 +129,9 @@ def library():
                 "lizard_feature_map_bwd": (I32, [FMP, P, P, P, P, P, P, SZ, P]),
                 "lizard_attn_fwd_bwd_host": (I32, [DP] + [P] * 8 + [I32, F] + [P] * 13 + [P, SZ, P]),
                 "lizard_selftest_wait_timeout": (I32, [P, SZ, ctypes.c_int64, P]),
+                "lizard_gate_workspace_bytes": (SZ, [GDP]),
+                "lizard_gate_fwd": (I32, [GDP, P, P, P, P]),
+                "lizard_gate_bwd": (I32, [GDP, P, P, P, P, P, P, SZ, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -212,6 +224,23 @@ def lizard_selftest_wait_timeout(workspace, wait_cycles: int, stream=None):
     _check(library().lizard_selftest_wait_timeout(_ptr(workspace), _ws_bytes(workspace),
                                                   int(wait_cycles), _stream(stream)),
            "lizard_selftest_wait_timeout")
+
+
+def lizard_gate_workspace_bytes(dims: lizard_gate_dims) -> int:
+    return library().lizard_gate_workspace_bytes(ctypes.byref(dims))
+
+
+def lizard_gate_fwd(dims: lizard_gate_dims, x, w, log_gamma, stream=None):
+    """log_gamma = logsigmoid(x W) / tau into preallocated ``log_gamma``."""
+    _check(library().lizard_gate_fwd(ctypes.byref(dims), _ptr(x), _ptr(w), _ptr(log_gamma),
+                                     _stream(stream)), "lizard_gate_fwd")
+
+
+def lizard_gate_bwd(dims: lizard_gate_dims, x, w, d_log_gamma, d_x, d_w, workspace, stream=None):
+    """d_x and d_w of the gate projection from d_log_gamma."""
+    _check(library().lizard_gate_bwd(ctypes.byref(dims), _ptr(x), _ptr(w), _ptr(d_log_gamma),
+                                     _ptr(d_x), _ptr(d_w), _ptr(workspace), _ws_bytes(workspace),
+                                     _stream(stream)), "lizard_gate_bwd")
 
 
 def _ws_bytes(ws):

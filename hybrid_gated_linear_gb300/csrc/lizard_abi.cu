@@ -591,6 +591,71 @@ lizard_status lizard_feature_map_bwd(const lizard_fmap_dims* dims, const void* x
   return cuda_status(e);
 }
 
+namespace {
+bool gate_dims_ok(const lizard_gate_dims* d) {
+  if (!d || d->B < 1 || d->H < 1 || d->L < 0 || d->D < 1 || d->D > 256) return false;
+  if (d->dk != 64 && d->dk != 128) return false;
+  if (d->dtype != LIZARD_F32 && d->dtype != LIZARD_BF16) return false;
+  if ((long long)d->B * d->H > 65535LL) return false;
+  if ((long long)d->B * d->H * (long long)d->L > (1LL << 40)) return false;
+  return isfinite(d->tau);
+}
+float resolve_tau(float tau) { return tau > 0.f ? tau : 16.f; }
+}  // namespace
+
+size_t lizard_gate_workspace_bytes(const lizard_gate_dims* dims) {
+  if (!gate_dims_ok(dims)) return 0;
+  return lz::align_up(lz::gate_bwd_workspace(dims->B, dims->H, dims->L, dims->D, dims->dk), 256);
+}
+
+lizard_status lizard_gate_fwd(const lizard_gate_dims* dims, const void* x, const void* w,
+                              float* log_gamma, void* stream) {
+  g_last_launches = 0;
+  if (!gate_dims_ok(dims)) return LIZARD_ERR_INVALID_ARG;
+  const lizard_gate_dims& d = *dims;
+  const bool tok = d.L > 0;
+  if (!ptr_ok(x, !tok) || !ptr_ok(w, false) || !ptr_ok(log_gamma, !tok)) return LIZARD_ERR_INVALID_ARG;
+  const size_t es = elem_size(d.dtype);
+  const size_t nx = (size_t)d.B * d.H * d.L * d.D * es, nw = (size_t)d.H * d.D * d.dk * es;
+  const size_t nl = (size_t)d.B * d.H * d.L * d.dk * sizeof(float);
+  if (overlap(log_gamma, nl, x, nx) || overlap(log_gamma, nl, w, nw)) return LIZARD_ERR_INVALID_ARG;
+  int launches = 0;
+  const cudaError_t e = lz::launch_gate_fwd(d.B, d.H, d.L, d.D, d.dk, d.dtype, resolve_tau(d.tau),
+                                            x, w, log_gamma, (cudaStream_t)stream, &launches);
+  g_last_launches = launches;
+  return cuda_status(e);
+}
+
+lizard_status lizard_gate_bwd(const lizard_gate_dims* dims, const void* x, const void* w,
+                              const float* d_log_gamma, void* d_x, float* d_w, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  g_last_launches = 0;
+  if (!gate_dims_ok(dims)) return LIZARD_ERR_INVALID_ARG;
+  const lizard_gate_dims& d = *dims;
+  const bool tok = d.L > 0;
+  if (!ptr_ok(x, !tok) || !ptr_ok(w, false) || !ptr_ok(d_log_gamma, !tok) || !ptr_ok(d_x, !tok) ||
+      !ptr_ok(d_w, false))
+    return LIZARD_ERR_INVALID_ARG;
+  const size_t need = lizard_gate_workspace_bytes(dims);
+  if (tok && (!workspace || workspace_bytes < need || !aligned16(workspace))) return LIZARD_ERR_WORKSPACE;
+  const size_t es = elem_size(d.dtype);
+  const size_t nx = (size_t)d.B * d.H * d.L * d.D * es, nw = (size_t)d.H * d.D * d.dk * es;
+  const size_t nl = (size_t)d.B * d.H * d.L * d.dk * sizeof(float);
+  const size_t ndw = (size_t)d.H * d.D * d.dk * sizeof(float);
+  struct Span { const void* p; size_t n; };
+  const Span ins[] = {{x, nx}, {w, nw}, {d_log_gamma, nl}, {workspace, workspace_bytes}};
+  for (const Span& in : ins)
+    if (overlap(d_x, nx, in.p, in.n) || overlap(d_w, ndw, in.p, in.n)) return LIZARD_ERR_INVALID_ARG;
+  if (overlap(d_x, nx, d_w, ndw)) return LIZARD_ERR_INVALID_ARG;
+  int launches = 0;
+  const cudaError_t e = lz::launch_gate_bwd(d.B, d.H, d.L, d.D, d.dk, d.dtype, resolve_tau(d.tau),
+                                            x, w, d_log_gamma, d_x, d_w,
+                                            static_cast<unsigned char*>(workspace),
+                                            (cudaStream_t)stream, &launches);
+  g_last_launches = launches;
+  return cuda_status(e);
+}
+
 size_t lizard_fwd_bwd_host_workspace_bytes(const lizard_dims* dims, int32_t W) {
   if (!dims_ok(dims) || W < 1 || shape_supported(dims->dk, dims->dv) != LIZARD_OK) return 0;
   const int Hs = host_slice_heads(dims->H);

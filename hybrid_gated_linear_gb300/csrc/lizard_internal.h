@@ -262,6 +262,14 @@ cudaError_t launch_fmap_bwd(int B, int H, int L, int D, int F, lizard_dtype dt, 
                             const void* w, const void* dphi, void* dx, float* dw,
                             unsigned char* ws, unsigned* status, cudaStream_t s, int* launches);
 
+// Gate projection log gamma = logsigmoid(x W) / tau and its backward (k_gate.cu).
+size_t gate_bwd_workspace(int B, int H, int L, int D, int dk);
+cudaError_t launch_gate_fwd(int B, int H, int L, int D, int dk, lizard_dtype dt, float tau,
+                            const void* x, const void* w, float* lg, cudaStream_t s, int* launches);
+cudaError_t launch_gate_bwd(int B, int H, int L, int D, int dk, lizard_dtype dt, float tau,
+                            const void* x, const void* w, const float* dlg, void* dx, float* dw,
+                            unsigned char* ws, cudaStream_t s, int* launches);
+
 cudaError_t launch_state_combine(int units, int dk, int dv, const float* ga, const float* ha,
                                  const float* gb, const float* hb, float* go, float* ho,
                                  cudaStream_t s, int* launches);

@@ -320,6 +320,35 @@ lizard_status lizard_workspace_init(void* workspace, size_t workspace_bytes, voi
 lizard_status lizard_check_device_errors(void* workspace, void* stream);
 
 /*
+ * Gate projection in front of the operator ("Lizard", arXiv 2507.09025, Method: the gate
+ * projection W_gamma is trained; papernotes.org note, 关键设计: gamma_i is computed by
+ * W_gamma).  The pages fix neither the projection's input nor its nonlinearity; this
+ * library takes the form of the workloads' gates:
+ *   log_gamma[b,h,t,k] = logsigmoid( sum_d x[b,h,t,d] W[h,d,k] ) / tau
+ * so every gamma lies in (0, 1); tau > 0 is a temperature (tau <= 0 selects 16).
+ *   x [B,H,L,D] T (D in 1..256); w [H,D,dk] T (dk = 64 or 128); log_gamma [B,H,L,dk]
+ *   fp32 output, the operator's log_gamma input.
+ * The backward takes d_log_gamma [B,H,L,dk] fp32 (from lizard_attn_bwd) and returns
+ *   d_x [B,H,L,D] T and d_w [H,D,dk] fp32, the latter summed over batch and tokens in a
+ *   fixed order (run-to-run identical); its workspace is lizard_gate_workspace_bytes
+ *   (caller-owned, 16-byte aligned; the forward needs none and may pass NULL, 0).
+ * CUDA cores, fp32 arithmetic.
+ */
+typedef struct lizard_gate_dims {
+    int32_t B, H, L;      /* batch, heads, tokens (L >= 0) */
+    int32_t D;            /* input features, 1..256 */
+    int32_t dk;           /* key dimension: 64 or 128 */
+    lizard_dtype dtype;   /* element type of x, w, d_x */
+    float tau;            /* temperature; <= 0 selects 16 */
+} lizard_gate_dims;
+size_t lizard_gate_workspace_bytes(const lizard_gate_dims* dims);
+lizard_status lizard_gate_fwd(const lizard_gate_dims* dims, const void* x, const void* w,
+                              float* log_gamma, void* stream);
+lizard_status lizard_gate_bwd(const lizard_gate_dims* dims, const void* x, const void* w,
+                              const float* d_log_gamma, void* d_x, float* d_w, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
  * Self-test of the device-side failure detection (a library service; the pages have no
  * counterpart).  Every wait of the tile kernels on an mbarrier is bounded: when it runs
  * out the CTA stops its other roles, drains what it has in flight, frees its tensor

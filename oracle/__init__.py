@@ -211,3 +211,28 @@ def feature_map_bwd(x, w, d_phi):
     dx = np.einsum("bhlf,hdf->bhld", dz, ww)
     dw = np.einsum("bhld,bhlf->hdf", xx, dz)
     return dx, dw
+
+
+def _logsigmoid(z):
+    return np.where(z >= 0, -np.log1p(np.exp(-z)), z - np.log1p(np.exp(z)))
+
+
+def gate(x, w, tau=16.0):
+    """Gate projection ("Lizard", arXiv 2507.09025, Method: the trained gate projection
+    W_gamma; papernotes.org note, 关键设计: gamma_i from W_gamma), in the form the library
+    takes: log gamma = logsigmoid(x W) / tau with x [B,H,L,D] and per-head W [H,D,dk].
+    fp64 numpy."""
+    z = np.einsum("bhld,hdk->bhlk", _f64(x), _f64(w))
+    return _logsigmoid(z) / tau
+
+
+def gate_bwd(x, w, d_log_gamma, tau=16.0):
+    """Adjoint of :func:`gate`: with z = x W, d logsigmoid(z)/dz = sigmoid(-z), so
+    dz = d_log_gamma sigmoid(-z) / tau, dx = dz W^T and dW[h] = sum over batch and tokens
+    of x^T dz.  Returns (dx, dW)."""
+    xx, ww, dl = _f64(x), _f64(w), _f64(d_log_gamma)
+    z = np.einsum("bhld,hdk->bhlk", xx, ww)
+    dz = dl / (1.0 + np.exp(z)) / tau
+    dx = np.einsum("bhlk,hdk->bhld", dz, ww)
+    dw = np.einsum("bhld,bhlk->hdk", xx, dz)
+    return dx, dw

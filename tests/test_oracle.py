@@ -459,3 +459,56 @@ def test_feature_map_gradients_match_finite_differences():
             lm = loss(m, Wt) if is_x else loss(X, m)
             fd = (lp - lm) / (2 * eps)
             assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (is_x, idx, fd, grad[idx])
+
+
+def _gate_small(B=1, H=2, L=4, D=5, dk=3, seed=95):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((B, H, L, D)), rng.standard_normal((H, D, dk)) / np.sqrt(D),
+            rng.standard_normal((B, H, L, dk)))
+
+
+def test_gate_special_values():
+    """W = 0 gives logsigmoid(0)/tau = -ln 2 / tau everywhere; a one-hot input row e_d
+    gives logsigmoid of row d of W; tau only divides; log gamma is negative, tends to 0
+    for large positive z and to z / tau for large negative z."""
+    X, Wt, _ = _gate_small()
+    np.testing.assert_allclose(oracle.gate(X, np.zeros_like(Wt), 16.0), -np.log(2.0) / 16.0,
+                               rtol=1e-15)
+    D = X.shape[-1]
+    one = np.zeros((1, Wt.shape[0], D, D))
+    for d in range(D):
+        one[0, :, d, d] = 1.0
+    g1 = oracle.gate(one, Wt, 1.0)
+    for h in range(Wt.shape[0]):
+        for d in range(D):
+            for k in range(Wt.shape[-1]):
+                z = Wt[h, d, k]
+                assert g1[0, h, d, k] == pytest.approx(-np.log(1.0 + np.exp(-z)), rel=1e-14)
+    np.testing.assert_allclose(oracle.gate(X, Wt, 4.0) * 4.0, oracle.gate(X, Wt, 1.0), rtol=1e-14)
+    assert (oracle.gate(X, Wt) < 0).all()
+    big = np.full((1, 1, 1, 1), 50.0)
+    assert abs(oracle.gate(big, np.ones((1, 1, 1)), 1.0)[0, 0, 0, 0]) < 1e-20
+    assert oracle.gate(-big, np.ones((1, 1, 1)), 2.0)[0, 0, 0, 0] == pytest.approx(-25.0, rel=1e-15)
+
+
+def test_gate_gradients_match_finite_differences():
+    """loss = sum(gate(x; W) * G): central differences in every entry of x and W against
+    gate_bwd(x, W, G)."""
+    X, Wt, G = _gate_small(seed=96)
+    dx, dw = oracle.gate_bwd(X, Wt, G, 3.0)
+
+    def loss(Xa, Wa):
+        return float((oracle.gate(Xa, Wa, 3.0) * G).sum())
+
+    eps = 1e-6
+    for arr, grad, is_x in ((X, dx, True), (Wt, dw, False)):
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            p, m = arr.copy(), arr.copy()
+            p[idx] += eps
+            m[idx] -= eps
+            lp = loss(p, Wt) if is_x else loss(X, p)
+            lm = loss(m, Wt) if is_x else loss(X, m)
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (is_x, idx, fd, grad[idx])
