@@ -188,17 +188,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecArgs a) {
 //  * decode_gla_kernel streams the fp32 state (128 KiB of the 166 KiB a unit moves):
 //    every thread issues its sixteen 16-byte state loads before anything else, three
 //    CTAs share an SM, and y_gla goes to y.
-//  * decode_win_kernel stages the two rings in shared memory (keys and values in two
-//    copy groups), computes the window softmax (8 lanes per key, lanes interleaved over
-//    dimensions so the shared-memory reads are conflict-free), adds alpha * y_win into y,
-//    writes the new token into its slot and advances pos (last CTA of each sequence).
-//    It is launched as a programmatic dependent of decode_gla_kernel, whose outputs it
-//    reads only after griddepcontrol.wait: its ring copies run during the state pass's
-//    tail (a 64 x 32 step measured 67 -> 62 us).
+//  * decode_win_kernel takes one warp per (sequence, head): the logits over the meta
+//    tokens, the ring and the new token, the softmax and y_win in registers and a small
+//    per-warp shared row, then adds alpha * y_win into y, writes the new token into its
+//    slot and advances pos (last warp of each sequence).  It is launched as a
+//    programmatic dependent of decode_gla_kernel, whose outputs it reads only after
+//    griddepcontrol.wait, so all of its ring reads overlap the state pass.
 // ------------------------------------------------------------------------------------
 constexpr int kSplitMaxW = 128;
-constexpr int kWinThreads = 256;
-constexpr int kWinWarps = kWinThreads / 32;
 
 template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 3) decode_gla_kernel(DecArgs a) {
@@ -257,144 +254,148 @@ __global__ void __launch_bounds__(kThreads, 3) decode_gla_kernel(DecArgs a) {
   }
 }
 
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
-               "l"(gsrc)
-               : "memory");
+// One warp per (sequence, head): lane l owns dimensions [l DPL, (l+1) DPL) of every key,
+// value, q and y row, so each row is one coalesced load of the warp.  No CTA barrier and
+// little register state, so all N*H units are resident at once and the kernel runs at
+// the rings' bandwidth; everything before griddepcontrol.wait overlaps the state kernel.
+constexpr int kWinUnits = 8;  // warps (units) per CTA
+constexpr int kWinRows = kMaxM + kSplitMaxW + 1;
+
+template <typename T, int DPL>
+__device__ __forceinline__ void ld_row(const T* p, float (&v)[DPL]) {
+  if constexpr (DPL == 4) {
+    const float4 f = ld4(p);
+    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) v[i] = ld_f(p + i);
+  }
 }
 
-template <typename T, int DK, int DV>
-__global__ void __launch_bounds__(kWinThreads) decode_win_kernel(DecArgs a) {
-  extern __shared__ __align__(128) unsigned char wsm[];
-  const int W = a.W, M = a.M;
-  // keys: W ring rows, M meta rows, then the new token's row; values likewise, so one
-  // row index serves both.  The new token has a row of its own, which no ring copy
-  // targets, so it needs no ordering against them.
-  T* skey = reinterpret_cast<T*>(wsm);            // [W + M + 1][DK]
-  T* sval = skey + (size_t)(W + M + 1) * DK;      // [W + M + 1][DV]
-  __shared__ __align__(16) float s_q[DK];
-  __shared__ float s_z[kMaxM + kSplitMaxW];
-  __shared__ int s_row[kMaxM + kSplitMaxW];
-  __shared__ float s_part[kWinThreads / DV > 0 ? kWinThreads / DV : 1][DV];
-  __shared__ int64_t s_pos;
-  const int u = blockIdx.x;
-  const int n = u / a.H, hh = u % a.H;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  T* kr = static_cast<T*>(a.kr) + (size_t)u * W * DK;
-  T* vr = static_cast<T*>(a.vr) + (size_t)u * W * DV;
-  const T* kg = static_cast<const T*>(a.k) + (size_t)u * DK;
-  const T* vg = static_cast<const T*>(a.v) + (size_t)u * DV;
-  if (tid == 0) s_pos = a.pos[n];
-  {
-    // asynchronous 16-byte copies of both rings and this head's meta rows
-    constexpr int KC = DK * sizeof(T) / 16, VC = DV * sizeof(T) / 16;  // 16-B chunks per row
-    const T* mkp = static_cast<const T*>(a.mk) + (size_t)hh * M * DK;
-    const T* mvp = static_cast<const T*>(a.mv) + (size_t)hh * M * DV;
-    for (int e = tid; e < W * KC; e += kWinThreads) cp_async16(skey + e * (16 / sizeof(T)), kr + e * (16 / sizeof(T)));
-    for (int e = tid; e < M * KC; e += kWinThreads)
-      cp_async16(skey + (size_t)W * DK + e * (16 / sizeof(T)), mkp + e * (16 / sizeof(T)));
-    asm volatile("cp.async.commit_group;" ::: "memory");  // keys: the logits need only these
-    for (int e = tid; e < W * VC; e += kWinThreads) cp_async16(sval + e * (16 / sizeof(T)), vr + e * (16 / sizeof(T)));
-    for (int e = tid; e < M * VC; e += kWinThreads)
-      cp_async16(sval + (size_t)W * DV + e * (16 / sizeof(T)), mvp + e * (16 / sizeof(T)));
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  }
-  const T* qg = static_cast<const T*>(a.q) + (size_t)u * DK;
-  T* y = static_cast<T*>(a.y) + (size_t)u * DV;
-  const int nrow = W + M;  // the new token's row
-  for (int d = tid; d < DK; d += kWinThreads) {
-    s_q[d] = ld_f(qg + d);
-    skey[(size_t)nrow * DK + d] = kg[d];
-  }
-  for (int c = tid; c < DV; c += kWinThreads) sval[(size_t)nrow * DV + c] = vg[c];
-  __syncthreads();
-  const int64_t p = s_pos;
-  const int slot = (int)(p % W);
-  // the new token replaces its slot in the global ring (the slot's old token is outside
-  // the window, so the copy of it in shared memory is never read)
-  for (int d = tid; d < DK; d += kWinThreads) kr[(size_t)slot * DK + d] = kg[d];
-  for (int c = tid; c < DV; c += kWinThreads) vr[(size_t)slot * DV + c] = vg[c];
-  const int64_t t_lo = p - W + 1 > 0 ? p - W + 1 : 0;
-  const int nkeys = M + (int)(p - t_lo + 1);
-  // row of key j: meta keys first (rows W..W+M-1), then window token t_lo + i at slot
-  // (t_lo + i) mod W, computed as one wrap of s_lo + i; the newest token (p) in its own row
-  const int s_lo = (int)(t_lo % W);
-  for (int j = tid; j < nkeys; j += kWinThreads) {
-    const int i = j - M, r = s_lo + i;
-    s_row[j] = j < M ? W + j : (j == nkeys - 1 ? nrow : (r >= W ? r - W : r));
-  }
-  asm volatile("cp.async.wait_group 1;" ::: "memory");  // this thread's key copies
-  __syncthreads();
-  {
-    // logits: 8 lanes per key, lane l8 takes dimensions {4*l8 + 32*i}
-    constexpr int LPK = 8;
-    const int sub = lane / LPK, l8 = lane % LPK;
-    for (int j0 = warp * 4; j0 < nkeys; j0 += kWinWarps * 4) {
-      const int j = j0 + sub;
-      float d = 0.f;
-      if (j < nkeys) {
-        const T* key = skey + (size_t)s_row[j] * DK;
+// Sum over the lanes of each of 8 values per lane in a fixed butterfly pattern; lane l
+// ends with the total of row ((l >> 4) & 1) * 4 + ((l >> 3) & 1) * 2 + ((l >> 2) & 1).
+__device__ __forceinline__ float warp_sum8(float (&v)[8]) {
+  const int lane = threadIdx.x & 31;
+  float w[8];
 #pragma unroll
-        for (int e = 4 * l8; e < DK; e += 32) {
-          const float4 q4 = *reinterpret_cast<const float4*>(s_q + e);
-          const float4 k4 = ld4(key + e);
-          d = fmaf(q4.x, k4.x, d);
-          d = fmaf(q4.y, k4.y, d);
-          d = fmaf(q4.z, k4.z, d);
-          d = fmaf(q4.w, k4.w, d);
-        }
-      }
+  for (int m = 0; m < 8; ++m) w[m] = v[m];
+  int off = 16;
 #pragma unroll
-      for (int o = LPK / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-      if (l8 == 0 && j < nkeys) s_z[j] = d * a.scale;
+  for (int nn = 8; nn > 1; nn >>= 1, off >>= 1) {
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int m = 0; m < nn / 2; ++m) {
+      const float send = up ? w[m] : w[m + nn / 2];
+      const float keep = up ? w[m + nn / 2] : w[m];
+      w[m] = keep + __shfl_xor_sync(0xffffffffu, send, off);
     }
   }
-  __syncthreads();
-  if (warp == 0) {
-    float mx = -INFINITY;
-    for (int j = lane; j < nkeys; j += 32) mx = fmaxf(mx, s_z[j]);
-    mx = warp_max(mx);
-    float sum = 0.f;
-    for (int j = lane; j < nkeys; j += 32) {
-      const float e = expf(s_z[j] - mx);
-      s_z[j] = e;
-      sum += e;
-    }
-    sum = warp_sum(sum);
-    const float inv = 1.f / sum;
-    for (int j = lane; j < nkeys; j += 32) s_z[j] *= inv;
-  }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");  // this thread's value copies
-  __syncthreads();
-  constexpr int NP = kWinThreads / DV > 0 ? kWinThreads / DV : 1;  // key partitions
-  {
-    const int c = tid % DV, part = tid / DV;
-    if (part < NP) {
-      float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
-      int j = part;
-      for (; j + 3 * NP < nkeys; j += 4 * NP) {
-        y0 = fmaf(s_z[j], ld_f(sval + (size_t)s_row[j] * DV + c), y0);
-        y1 = fmaf(s_z[j + NP], ld_f(sval + (size_t)s_row[j + NP] * DV + c), y1);
-        y2 = fmaf(s_z[j + 2 * NP], ld_f(sval + (size_t)s_row[j + 2 * NP] * DV + c), y2);
-        y3 = fmaf(s_z[j + 3 * NP], ld_f(sval + (size_t)s_row[j + 3 * NP] * DV + c), y3);
+  float x = w[0];
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  return x;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kWinUnits * 32) decode_win_kernel(DecArgs a) {
+  constexpr int DPL = D / 32;
+  __shared__ float s_z[kWinUnits][kWinRows];  // logits, then probabilities
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x * kWinUnits + warp;
+  if (u >= a.N * a.H) return;
+  const int n = u / a.H, hh = u % a.H, W = a.W, M = a.M;
+  const int R = M + W + 1;  // rows: the meta tokens, the W ring slots, the new token
+  const int d0 = lane * DPL;
+  T* kr = static_cast<T*>(a.kr) + (size_t)u * W * D;
+  T* vr = static_cast<T*>(a.vr) + (size_t)u * W * D;
+  const T* mk = static_cast<const T*>(a.mk) + (size_t)hh * M * D;
+  const T* mv = static_cast<const T*>(a.mv) + (size_t)hh * M * D;
+  float q[DPL], kn[DPL], vn[DPL];
+  ld_row<T, DPL>(static_cast<const T*>(a.q) + (size_t)u * D + d0, q);
+  ld_row<T, DPL>(static_cast<const T*>(a.k) + (size_t)u * D + d0, kn);
+  ld_row<T, DPL>(static_cast<const T*>(a.v) + (size_t)u * D + d0, vn);
+  const int64_t p = a.pos[n];
+  // ring slot s holds token t with t mod W = s; the window is [max(0, p-W+1), p], whose
+  // token p (the new one) replaces slot p mod W: every other written slot is in it
+  const int sp = (int)(p % W);
+  auto valid = [&](int r) {
+    if (r < M || r == R - 1) return true;
+    const int sl = r - M;
+    return p >= W ? sl != sp : sl < (int)p;
+  };
+  auto krow = [&](int r) -> const T* { return r < M ? mk + (size_t)r * D : kr + (size_t)(r - M) * D; };
+  auto vrow = [&](int r) -> const T* { return r < M ? mv + (size_t)r * D : vr + (size_t)(r - M) * D; };
+  float* z = s_z[warp];
+
+  // logits, sixteen rows (two reductions of eight) at a time
+  for (int r0 = 0; r0 < R; r0 += 16) {
+    float part[2][8];
+    // every load is issued unconditionally (rows past the ring read its last row and are
+    // replaced afterwards), so the sixteen loads are in flight together
+    float kv[16][DPL];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) ld_row<T, DPL>(krow(min(r0 + e, R - 2)) + d0, kv[e]);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int r = r0 + e;
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) {
+        const float k = r < R - 1 ? kv[e][i] : (r == R - 1 ? kn[i] : 0.f);
+        acc = fmaf(q[i], k, acc);
       }
-      for (; j < nkeys; j += NP) y0 = fmaf(s_z[j], ld_f(sval + (size_t)s_row[j] * DV + c), y0);
-      s_part[part][c] = (y0 + y1) + (y2 + y3);
+      part[e >> 3][e & 7] = acc;
+    }
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const float tot = warp_sum8(part[hf]);
+      const int r = r0 + 8 * hf + ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+      if ((lane & 3) == 0 && r < R) z[r] = valid(r) ? tot * a.scale : -INFINITY;
     }
   }
-  __syncthreads();
-  // y_gla comes from the GLA kernel launched just before this one (programmatic
-  // dependent launch: everything above overlaps that kernel's tail)
+  __syncwarp();
+  float mx = -INFINITY;
+  for (int r = lane; r < R; r += 32) mx = fmaxf(mx, z[r]);
+  mx = warp_max(mx);
+  float sum = 0.f;
+  for (int r = lane; r < R; r += 32) {
+    const float e = expf(z[r] - mx);  // 0 for the rows outside the window
+    z[r] = e;
+    sum += e;
+  }
+  sum = warp_sum(sum);
+  __syncwarp();
+  // y_win = sum_r p_r value_r, eight rows at a time
+  float yw[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) yw[i] = 0.f;
+  for (int r0 = 0; r0 < R; r0 += 16) {
+    float vv[16][DPL];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) ld_row<T, DPL>(vrow(min(r0 + e, R - 2)) + d0, vv[e]);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int r = r0 + e;
+      const float pr = r < R ? z[r] : 0.f;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) yw[i] = fmaf(pr, r < R - 1 ? vv[e][i] : vn[i], yw[i]);
+    }
+  }
+  // the new token into its slot (this warp read that slot's old content above)
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) {
+    kr[(size_t)sp * D + d0 + i] = static_cast<const T*>(a.k)[(size_t)u * D + d0 + i];
+    vr[(size_t)sp * D + d0 + i] = static_cast<const T*>(a.v)[(size_t)u * D + d0 + i];
+  }
+  // y_gla comes from the state kernel launched just before this one (programmatic
+  // dependent launch: everything above overlaps that kernel)
   pdl_wait();
-  for (int c = tid; c < DV; c += kWinThreads) {
-    float ys = 0.f;
+  const float inv = a.alpha / sum;
+  T* y = static_cast<T*>(a.y) + (size_t)u * D + d0;
 #pragma unroll
-    for (int r = 0; r < NP; ++r) ys += s_part[r][c];
-    y[c] = cvt_out<T>(ld_f(y + c) + a.alpha * ys);
-  }
-  __syncthreads();
-  if (tid == 0) {
+  for (int i = 0; i < DPL; ++i) y[i] = cvt_out<T>(ld_f(y + i) + inv * yw[i]);
+  __syncwarp();
+  if (lane == 0) {
     __threadfence();
     const unsigned prev = atomicAdd(&a.counters[n], 1u);
     if (prev == (unsigned)a.H - 1) {
@@ -415,12 +416,10 @@ cudaError_t launch_typed(const DecArgs& a, cudaStream_t s, int* launches) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++*launches;
-    const size_t smem = (size_t)(a.W + a.M + 1) * 2 * D * sizeof(T);
-    e = cudaFuncSetAttribute(decode_win_kernel<T, D, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
+    const int units = a.N * a.H;
     trace_begin("decode_win", s);
-    e = launch_pdl(decode_win_kernel<T, D, D>, dim3(a.N * a.H), dim3(kWinThreads), smem, s, a);
+    e = launch_pdl(decode_win_kernel<T, D>, dim3((units + kWinUnits - 1) / kWinUnits),
+                   dim3(kWinUnits * 32), 0, s, a);
     trace_end(s);
     if (e != cudaSuccess) return e;
   } else {
