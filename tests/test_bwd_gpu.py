@@ -56,14 +56,19 @@ def test_bwd_is_deterministic():
 
 def test_training_workload_sampled_head():
     """B=8, L=2048, H=32, d=128 in the shipped launch configuration.  Head 3 is recomputed
-    by the oracle for all 8 batch entries (the meta gradients sum over the batch)."""
+    by the oracle for all 8 batch entries (the meta gradients sum over the batch); the
+    forward's y of that head is compared too."""
+    from gpu_util import gpu_fwd
     w = synth.WORKLOADS["train_fwd_bwd"]
     x = synth.workload_inputs("train_fwd_bwd")
+    y, _ = gpu_fwd(x, w["W"], "bf16")
     g = gpu_bwd(x, w["W"], "bf16")
     h = 3
     sub = {n: x[n][:, h:h + 1] for n in ("phi_q", "phi_k", "v", "log_gamma", "q", "k", "dy")}
-    ref = oracle.bwd(*(sub[n] for n in ("phi_q", "phi_k", "v", "log_gamma", "q", "k")),
-                     x["meta_k"][h:h + 1], x["meta_v"][h:h + 1], sub["dy"], W=w["W"])
+    args = [sub[n] for n in ("phi_q", "phi_k", "v", "log_gamma", "q", "k")]
+    yref = oracle.fwd(*args, x["meta_k"][h:h + 1], x["meta_v"][h:h + 1], W=w["W"])["y"]
+    assert rel_l2(y[:, h:h + 1], yref) <= TOL["bf16"]
+    ref = oracle.bwd(*args, x["meta_k"][h:h + 1], x["meta_v"][h:h + 1], sub["dy"], W=w["W"])
     errs = {}
     for n in GRADS:
         got = g[n][h:h + 1] if n.startswith("d_meta") else g[n][:, h:h + 1]
