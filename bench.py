@@ -778,25 +778,31 @@ def run_ours(args):
                          "right after the timed region (the event pairs keep consecutive "
                          "kernels from overlapping, so this pass runs slower than the timed one)",
     }
-    try:
-        parts["decode"] = _decode_part(dev, stream, peaks)
-    except Exception as e:  # reported, never hidden
-        parts["decode"] = {"error": repr(e)}
-    try:
-        parts["feature_map"] = _fmap_part(dev, peaks, flush, prob)
-    except Exception as e:  # reported, never hidden
-        parts["feature_map"] = {"error": repr(e)}
-    try:
-        xl = _long_context_inputs()
-        for key, H in (("long_context", 32), ("long_context_split", 4)):
-            try:
-                parts[key] = _long_context_part(dev, peaks, flush, xl, H=H)
-            except Exception as e:  # reported, never hidden
-                parts[key] = {"error": repr(e)}
-        del xl
-    except Exception as e:  # reported, never hidden
-        parts["long_context"] = {"error": repr(e)}
-    if not args.no_train_part:
+    want = set(args.parts.split(",")) if args.parts else set()
+    if "train" in want and args.no_train_part:
+        want.discard("train")
+    if "decode" in want:
+        try:
+            parts["decode"] = _decode_part(dev, stream, peaks)
+        except Exception as e:  # reported, never hidden
+            parts["decode"] = {"error": repr(e)}
+    if "fmap" in want:
+        try:
+            parts["feature_map"] = _fmap_part(dev, peaks, flush, prob)
+        except Exception as e:  # reported, never hidden
+            parts["feature_map"] = {"error": repr(e)}
+    if "long" in want:
+        try:
+            xl = _long_context_inputs()
+            for key, H in (("long_context", 32), ("long_context_split", 4)):
+                try:
+                    parts[key] = _long_context_part(dev, peaks, flush, xl, H=H)
+                except Exception as e:  # reported, never hidden
+                    parts[key] = {"error": repr(e)}
+            del xl
+        except Exception as e:  # reported, never hidden
+            parts["long_context"] = {"error": repr(e)}
+    if "train" in want:
         try:
             parts["train_step"] = _train_part(dev, peaks, flush, args.steps)
         except Exception as e:  # reported, never hidden
@@ -850,6 +856,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-train-part", action="store_true",
                     help="skip the training-workload line in parts (a shorter run)")
+    ap.add_argument("--parts", default="decode,fmap,long,train",
+                    help="comma list of the extra sections measured after the step: decode, "
+                         "fmap, long (long context), train (the B=8 L=2048 step); '' for none")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

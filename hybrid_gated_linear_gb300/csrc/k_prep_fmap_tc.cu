@@ -49,19 +49,6 @@ struct PfParams {
   unsigned* wcount;
 };
 
-// Named barrier over n threads that also returns whether v was true in any of them.
-__device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
-  __syncwarp();
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(v ? 1u : 0u), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-
 enum { P_LD = 0, P_Z, P_DONE, P_COUNT };
 // x_q, x_k 32 KB each (then the Qt, Kt staging); W_q, W_k 16 KB each (then the e^b
 // staging); the log-gate tile 64 KB fp32 (four 32-column blocks), turned into b in place

@@ -37,12 +37,14 @@ constexpr int kD = 128;   // dk = dv
 constexpr int kBand = 192;
 constexpr int kMetaRows = 16;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kThreads = 6 * 32;  // warp 0 TMA, warp 1 MMA, warps 2-5 rows
+// warp 0 TMA, warp 1 MMA, then kParts warps per TMEM lane quadrant for the row work
+constexpr int kParts = 4;
+constexpr int kThreads = 64 + kParts * 128;
 
 using Ctl = tc::Ctl<8>;
 
 struct Params {
-  int H, L, M, W, nq;
+  int H, L, M, W, nq, nbh;
   int ahead;  // CTAs per wave: the tile whose inputs a CTA prefetches into L2
   float scale, alpha;
   float* lse2;      // [BH][L]  log2-domain log-sum-exp of each query row
@@ -51,6 +53,8 @@ struct Params {
   const float* dvacc;  // [BH][L][128] GLA part of dv
   bf16 *dq, *dk, *dv;
   unsigned* status;
+  unsigned* tiles;  // query kernel: [0] next block to hand out, [1] CTAs done (both 0
+                    // between launches: the last CTA to finish sets them back)
 };
 
 // ------------------------------------------------------------------------------------
@@ -61,11 +65,22 @@ struct QMaps {
   CUtensorMap dqo;                    // store
 };
 
-enum { Q_LDK = 0, Q_LDV, Q_ZF, Q_DPF, Q_DS, Q_OUT, Q_DONE };
+// The query kernel is persistent: one CTA per SM takes query blocks from a counter in
+// global memory until none is left (so CTAs that start late, behind the GLA kernels on the
+// other stream, simply take fewer).  The loads of the next block start as soon as the MMAs
+// of the current one have read their operands, and its logits as soon as the rows have
+// read dQ out of TMEM, so copy-in, tensor-core and row phases of consecutive blocks
+// overlap; dq leaves through a staging tile of its own.  The TMA thread passes each block
+// index (or -1 at the end) to the other roles through a two-slot ring in shared memory,
+// published by the arrival on Q_LDK.
+enum { Q_LDK = 0, Q_LDV, Q_ZF, Q_DPF, Q_DS, Q_OUT, Q_TMF, Q_DONE };
 constexpr uint32_t QS_Q = 0, QS_DY = 32768, QS_KB = 65536, QS_VB = QS_KB + 49152,
                    QS_KM = QS_VB + 49152, QS_VM = QS_KM + 4096, QS_DSM = QS_VM + 4096,
-                   QS_PM = QS_DSM + 4096, QS_BARS = QS_PM + 4096;
+                   QS_PM = QS_DSM + 4096, QS_DQS = QS_PM + 4096, QS_RED = QS_DQS + 32768,
+                   QS_BARS = QS_RED + 3 * kParts * 128 * 4;
 constexpr size_t kQSmem = QS_BARS + 1024 + 1024;
+static_assert(kQSmem <= 232448, "query kernel shared memory");
+static_assert(sizeof(Ctl) <= 512, "barrier block below the block-index ring");
 // TMEM columns: Z 0..207, dP 208..415, dMk 416, dMv 432; dQ reuses 0..127.
 constexpr uint32_t TQ_Z = 0, TQ_DP = 208, TQ_MK = 416, TQ_MV = 432, TQ_DQ = 0;
 
@@ -76,13 +91,13 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Ctl* ctl = reinterpret_cast<Ctl*>(sm + QS_BARS);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qb = blockIdx.x % p.nq, bh = blockIdx.x / p.nq;
-  const int hh = bh % p.H;
   const int L = p.L, M = p.M, W = p.W;
-  const int i0 = qb * kB;
+  const int ntiles = p.nbh * p.nq;
+  volatile int* tslot = reinterpret_cast<volatile int*>(sm + QS_BARS + 512);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i <= Q_DONE; ++i) mbar_init(&ctl->bar[i], i == Q_DS ? 128u : 1u);
+    for (int i = 0; i <= Q_DONE; ++i)
+      mbar_init(&ctl->bar[i], (i == Q_DS || i == Q_TMF) ? kParts * 128u : 1u);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -99,38 +114,53 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
   if (warp == 0) {
     if (lane == 0) {
       const uint32_t meta_bytes = M > 0 ? 2u * kMetaRows * 128u : 0u;
-      mbar_arrive_expect_tx(&ctl->bar[Q_LDK], 32768 + 49152 + meta_bytes);
-      tma_load_3d(sm + QS_Q, &maps.q, 0, i0, bh, &ctl->bar[Q_LDK]);
-      tma_load_3d(sm + QS_Q + 16384, &maps.q, 64, i0, bh, &ctl->bar[Q_LDK]);
-      tma_load_3d(sm + QS_KB, &maps.kb, 0, i0 - 64, bh, &ctl->bar[Q_LDK]);
-      tma_load_3d(sm + QS_KB + 24576, &maps.kb, 64, i0 - 64, bh, &ctl->bar[Q_LDK]);
-      if (M > 0) {
-        tma_load_3d(sm + QS_KM, &maps.mk, 0, 0, hh, &ctl->bar[Q_LDK]);
-        tma_load_3d(sm + QS_KM + 2048, &maps.mk, 64, 0, hh, &ctl->bar[Q_LDK]);
-      }
-      mbar_arrive_expect_tx(&ctl->bar[Q_LDV], 32768 + 49152 + meta_bytes);
-      tma_load_3d(sm + QS_DY, &maps.dy, 0, i0, bh, &ctl->bar[Q_LDV]);
-      tma_load_3d(sm + QS_DY + 16384, &maps.dy, 64, i0, bh, &ctl->bar[Q_LDV]);
-      tma_load_3d(sm + QS_VB, &maps.vb, 0, i0 - 64, bh, &ctl->bar[Q_LDV]);
-      tma_load_3d(sm + QS_VB + 24576, &maps.vb, 64, i0 - 64, bh, &ctl->bar[Q_LDV]);
-      if (M > 0) {
-        tma_load_3d(sm + QS_VM, &maps.mv, 0, 0, hh, &ctl->bar[Q_LDV]);
-        tma_load_3d(sm + QS_VM + 2048, &maps.mv, 64, 0, hh, &ctl->bar[Q_LDV]);
-      }
-      // warm L2 with the inputs of the tile one wave later
-      const int nb = blockIdx.x + p.ahead;
-      if (nb < gridDim.x && wait_bar(ctl, Q_LDV, 0)) {
-        const int nbh = nb / p.nq, ni0 = (nb % p.nq) * kB;
-        for (int x = 0; x < kD; x += 64) {
-          tma_prefetch_l2_3d(&maps.q, x, ni0, nbh);
-          tma_prefetch_l2_3d(&maps.kb, x, ni0 - 64, nbh);
-          tma_prefetch_l2_3d(&maps.dy, x, ni0, nbh);
-          tma_prefetch_l2_3d(&maps.vb, x, ni0 - 64, nbh);
+      uint32_t nk = 0, nv = 0;  // phases armed on Q_LDK and Q_LDV
+      int t = (int)atomicAdd(p.tiles, 1u);
+      while (true) {
+        // the previous block's MMAs have read Q, dY, the bands and the ds tiles
+        if (nk > 0 && !wait_bar(ctl, Q_OUT, (nk - 1) & 1)) break;
+        tslot[nk & 1] = t < ntiles ? t : -1;
+        if (t >= ntiles) {
+          mbar_arrive(&ctl->bar[Q_LDK]);  // no copy: publishes the end mark
+          ++nk;
+          break;
+        }
+        const int bh = t / p.nq, i0 = (t % p.nq) * kB, hh = bh % p.H;
+        mbar_arrive_expect_tx(&ctl->bar[Q_LDK], 32768 + 49152 + meta_bytes);
+        tma_load_3d(sm + QS_Q, &maps.q, 0, i0, bh, &ctl->bar[Q_LDK]);
+        tma_load_3d(sm + QS_Q + 16384, &maps.q, 64, i0, bh, &ctl->bar[Q_LDK]);
+        tma_load_3d(sm + QS_KB, &maps.kb, 0, i0 - 64, bh, &ctl->bar[Q_LDK]);
+        tma_load_3d(sm + QS_KB + 24576, &maps.kb, 64, i0 - 64, bh, &ctl->bar[Q_LDK]);
+        if (M > 0) {
+          tma_load_3d(sm + QS_KM, &maps.mk, 0, 0, hh, &ctl->bar[Q_LDK]);
+          tma_load_3d(sm + QS_KM + 2048, &maps.mk, 64, 0, hh, &ctl->bar[Q_LDK]);
+        }
+        ++nk;
+        mbar_arrive_expect_tx(&ctl->bar[Q_LDV], 32768 + 49152 + meta_bytes);
+        tma_load_3d(sm + QS_DY, &maps.dy, 0, i0, bh, &ctl->bar[Q_LDV]);
+        tma_load_3d(sm + QS_DY + 16384, &maps.dy, 64, i0, bh, &ctl->bar[Q_LDV]);
+        tma_load_3d(sm + QS_VB, &maps.vb, 0, i0 - 64, bh, &ctl->bar[Q_LDV]);
+        tma_load_3d(sm + QS_VB + 24576, &maps.vb, 64, i0 - 64, bh, &ctl->bar[Q_LDV]);
+        if (M > 0) {
+          tma_load_3d(sm + QS_VM, &maps.mv, 0, 0, hh, &ctl->bar[Q_LDV]);
+          tma_load_3d(sm + QS_VM + 2048, &maps.mv, 64, 0, hh, &ctl->bar[Q_LDV]);
+        }
+        ++nv;
+        // take the next block now and warm L2 with its inputs
+        t = (int)atomicAdd(p.tiles, 1u);
+        if (t < ntiles && wait_bar(ctl, Q_LDV, (nv - 1) & 1)) {
+          const int nbh = t / p.nq, ni0 = (t % p.nq) * kB;
+          for (int x = 0; x < kD; x += 64) {
+            tma_prefetch_l2_3d(&maps.q, x, ni0, nbh);
+            tma_prefetch_l2_3d(&maps.kb, x, ni0 - 64, nbh);
+            tma_prefetch_l2_3d(&maps.dy, x, ni0, nbh);
+            tma_prefetch_l2_3d(&maps.vb, x, ni0 - 64, nbh);
+          }
         }
       }
       const uint64_t tw = globaltimer_ns();
-      drain_bar(ctl, Q_LDK, 1, tw);
-      drain_bar(ctl, Q_LDV, 1, tw);
+      drain_bar(ctl, Q_LDK, nk, tw);
+      drain_bar(ctl, Q_LDV, nv, tw);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -140,8 +170,13 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
       const uint32_t id_dq = idesc_bf16(kB, kD, false, true);
       const uint32_t id_dqm = idesc_bf16(kB, kD, true, true);
       const uint32_t id_meta = idesc_bf16(kD, kMetaRows, true, false);
-      bool ok = wait_bar(ctl, Q_LDK, 0);
-      if (ok) {
+      bool ok = true;
+      for (uint32_t k = 0;; ++k) {
+        if (!(ok = wait_bar(ctl, Q_LDK, k & 1))) break;
+        if (tslot[k & 1] < 0) break;
+        // Z overwrites the columns of the previous block's dQ: wait until the rows have
+        // read it
+        if (k > 0 && !(ok = wait_bar(ctl, Q_TMF, (k - 1) & 1))) break;
         tc_fence_after();
         if (M > 0)
           for (int j = 0; j < 8; ++j)
@@ -149,8 +184,7 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
         for (int j = 0; j < 8; ++j)
           mma_bf16(tmem + TQ_Z + 16, desc_k(sb + QS_Q, kB, j), desc_k(sb + QS_KB, kBand, j), id192, j > 0);
         mma_commit(&ctl->bar[Q_ZF]);
-      }
-      if (ok && (ok = wait_bar(ctl, Q_LDV, 0))) {
+        if (!(ok = wait_bar(ctl, Q_LDV, k & 1))) break;
         tc_fence_after();
         if (M > 0)
           for (int j = 0; j < 8; ++j)
@@ -158,8 +192,7 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
         for (int j = 0; j < 8; ++j)
           mma_bf16(tmem + TQ_DP + 16, desc_k(sb + QS_DY, kB, j), desc_k(sb + QS_VB, kBand, j), id192, j > 0);
         mma_commit(&ctl->bar[Q_DPF]);
-      }
-      if (ok && (ok = wait_bar(ctl, Q_DS, 0))) {
+        if (!(ok = wait_bar(ctl, Q_DS, k & 1))) break;
         tc_fence_after();
         // dQ = ds_band Kband (+ ds_meta Km); ds_band lives over the V band
         for (int j = 0; j < kBand / 16; ++j)
@@ -179,174 +212,199 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
       drain_bar(ctl, Q_DONE, 1, globaltimer_ns());
     }
   } else {
+    // kParts warps share each 32-lane TMEM quadrant: warp 2 + 4u + q reads lanes 32q..32q+31
+    // (q = warp mod 4) and takes the column groups g = u, u + kParts, ... of those rows.
     const int qw = warp & 3;
+    const int part = (warp - 2) >> 2;
     const int r = qw * 32 + lane;  // query row of the block
-    const int i = i0 + r;
-    const bool valid = i < L;
     const uint32_t tl = tmem + ((uint32_t)(qw * 32) << 16);
     const float zs = p.scale * kLog2e;
-    // band columns b <-> key j = i0 - 64 + b; this row sees b in [blo, bhi]
-    const int bhi = 64 + r;
-    const int blo = max(64 + r - W + 1, 64 - i0);
-    // 16-column band groups any row of this warp can see
+    const int nmeta = M > 0 ? 1 : 0;
+    // 16-column band groups any row of this quadrant can see (keys i0 - 64 + b)
     const int g_lo = max(0, 64 + 32 * qw - W + 1) >> 4;
     const int g_hi = (64 + 32 * qw + 31) >> 4;
-    const int nmeta = M > 0 ? 1 : 0;
-    const int ng = nmeta + g_hi - g_lo + 1;
-    auto zcol = [&](int g) { return g < nmeta ? 0 : 16 + 16 * (g_lo + g - nmeta); };
-    // visible columns of group g as a 16-bit mask (bits lo .. hi of the group)
-    auto vmask = [&](int g) -> uint32_t {
-      if (g < nmeta) return (1u << M) - 1u;  // M <= 16
-      const int base = 16 * (g_lo + g - nmeta);
-      const int lo = max(blo - base, 0), hi = min(bhi - base, 15);
-      return hi < lo ? 0u : ((0xffffu >> (15 - hi)) >> lo) << lo;
-    };
-    // The row's logits stay in registers for all three passes (at most one meta and six
-    // band groups when W <= 65), read from TMEM with a single wait; dP is read in two
-    // batches of four groups per pass.
-    constexpr int kNG = 7;
-    uint32_t z[kNG][16];
-    auto load_dp = [&](int h, uint32_t (&d)[4][16]) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (4 * h + k < kNG && 4 * h + k < ng) tmem_ld16(tl + TQ_DP + zcol(4 * h + k), d[k]);
-      tmem_ld_wait();
-    };
-    bool ok = wait_bar(ctl, Q_ZF, 0);
-    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    if (ok) {
-      tc_fence_after();
-#pragma unroll
-      for (int g = 0; g < kNG; ++g)
-        if (g < ng) tmem_ld16(tl + TQ_Z + zcol(g), z[g]);
-      tmem_ld_wait();
-      // logits this row does not see become -inf: the maximum needs no test, and
-      // 2^-inf = 0 stands for them in the sums below
-#pragma unroll
-      for (int g = 0; g < kNG; ++g)
-        if (g < ng) {
-          const uint32_t mk = vmask(g);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            if (!(mk & (1u << e))) z[g][e] = 0xff800000u;
-            m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(z[g][e]));
-          }
-        }
-    }
-    const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-    const float mxs = mx * zs;
-    float sum = 0.f, sdp = 0.f;
-    if (ok && (ok = wait_bar(ctl, Q_DPF, 0))) {
-      tc_fence_after();
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t d[4][16];
-        load_dp(h, d);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int g = 4 * h + k;
-          if (g < kNG && g < ng) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float ex = ex2_approx(fmaf(__uint_as_float(z[g][e]), zs, -mxs));
-              sum += ex;
-              sdp = fmaf(ex, __uint_as_float(d[k][e]), sdp);
-            }
-          }
-        }
-      }
-    }
-    const float lse2 = mxs + __log2f(sum);
-    const float Dv = p.alpha * sdp / sum;
+    const int nband = g_hi - g_lo + 1;  // at most 6 when W <= 65
+    // Group slots: band groups 0 .. nband-1, the meta group in slot 7, so that the warps
+    // taking slots 3 and 7 (and not those taking 0 and 4) do the meta stores.  Warp `part`
+    // takes the slots part and part + kParts.
+    constexpr int kMine = 8 / kParts;
+    auto slot_used = [&](int s) { return s < nband || (s == 7 && nmeta); };
+    auto zcol = [&](int s) { return s == 7 ? 0 : 16 + 16 * (g_lo + s); };
+    float* red = reinterpret_cast<float*>(sm + QS_RED);  // [3][kParts][128] partials
     unsigned char* dsb = sm + QS_VB;  // ds band tile, 128 rows x 192 columns
-    if (ok) {
+    bool ok = true;
+#pragma unroll 1
+    for (uint32_t k = 0;; ++k) {
+      // every row thread takes the same decision (the named barriers below need all)
+      const int t = (ok && (ok = wait_bar(ctl, Q_LDK, k & 1))) ? tslot[k & 1] : -1;
+      if (named_sync_or(1, kParts * 128, t < 0)) break;
+      const int qb = t % p.nq, bh = t / p.nq;
+      const int i0 = qb * kB;
+      const int i = i0 + r;
+      const bool valid = i < L;
+      // band columns b <-> key j = i0 - 64 + b; this row sees b in [blo, bhi]
+      const int bhi = 64 + r;
+      const int blo = max(64 + r - W + 1, 64 - i0);
+      auto vmask = [&](int s) -> uint32_t {
+        if (s == 7) return (1u << M) - 1u;  // M <= 16
+        const int base = 16 * (g_lo + s);
+        const int lo = max(blo - base, 0), hi = min(bhi - base, 15);
+        return hi < lo ? 0u : ((0xffffu >> (15 - hi)) >> lo) << lo;
+      };
+      // the staging tile is free once the previous block's dq store has read it; the
+      // named barriers below hold the other rows until then
+      if (threadIdx.x == 64) bulk_wait_read();
+      uint32_t z[kMine][16], d[kMine][16];
+      float mloc = -INFINITY;
+      if (ok && (ok = wait_bar(ctl, Q_ZF, k & 1))) {
+        tc_fence_after();
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t d[4][16];
-        load_dp(h, d);
+        for (int u = 0; u < kMine; ++u)
+          if (slot_used(part + u * kParts)) tmem_ld16(tl + TQ_Z + zcol(part + u * kParts), z[u]);
+        tmem_ld_wait();
+        // logits this row does not see become -inf: the maximum needs no test, and
+        // 2^-inf = 0 stands for them in the sums below
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int g = 4 * h + k;
-          if (g < kNG && g < ng) {
-            float ds[16], pp[16];
+        for (int u = 0; u < kMine; ++u)
+          if (slot_used(part + u * kParts)) {
+            const uint32_t mk = vmask(part + u * kParts);
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const float pe = valid ? ex2_approx(fmaf(__uint_as_float(z[g][e]), zs, -lse2)) : 0.f;
-              pp[e] = pe;
-              ds[e] = pe * fmaf(p.alpha, __uint_as_float(d[k][e]), -Dv);
-            }
-            if (g < nmeta) {
-              // transposed meta tiles: row m, column r
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                *reinterpret_cast<bf16*>(sm + QS_DSM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(ds[e]);
-                *reinterpret_cast<bf16*>(sm + QS_PM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(pp[e]);
-              }
-            } else {
-              store16_bf16(dsb, kB, r, 16 * (g_lo + g - nmeta), ds);
+              if (!(mk & (1u << e))) z[u][e] = 0xff800000u;
+              mloc = fmaxf(mloc, __uint_as_float(z[u][e]));
             }
           }
-        }
       }
-    }
-    // band groups no row of this warp sees hold zeros (the tile still holds V)
-    for (int g = 0; g < kBand / 16; ++g)
-      if (g < g_lo || g > g_hi) zero16_bf16(dsb, kB, r, 16 * g);
-    if (M == 0) {
+      red[part * 128 + r] = mloc;
+      named_sync(1, kParts * 128);
+      float mx = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        *reinterpret_cast<bf16*>(sm + QS_DSM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(0.f);
-        *reinterpret_cast<bf16*>(sm + QS_PM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(0.f);
-      }
-    }
-    tc_fence_before();
-    fence_proxy_async_smem();
-    mbar_arrive(&ctl->bar[Q_DS]);
-    if (ok && valid) {
-      p.lse2[(size_t)bh * L + i] = lse2;
-      p.Dw[(size_t)bh * L + i] = Dv;
-    }
-    if (ok && (ok = wait_bar(ctl, Q_OUT, 0))) {
-      tc_fence_after();
-      // dq staged over the query tile (free once the meta products are done)
-#pragma unroll 1
-      for (int c = 0; c < kD; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tl + TQ_DQ + c, v);
+      for (int u = 0; u < kParts; ++u) mx = fmaxf(mx, red[u * 128 + r]);
+      const float mxs = mx * zs;
+      // exponentials once: z[u][e] becomes 2^(z scale log2e - max)
+      float sum = 0.f, sdp = 0.f;
+      if (ok && (ok = wait_bar(ctl, Q_DPF, k & 1))) {
+        tc_fence_after();
+#pragma unroll
+        for (int u = 0; u < kMine; ++u)
+          if (slot_used(part + u * kParts)) tmem_ld16(tl + TQ_DP + zcol(part + u * kParts), d[u]);
         tmem_ld_wait();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int u = 0; u < kMine; ++u)
+          if (slot_used(part + u * kParts)) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float ex = ex2_approx(fmaf(__uint_as_float(z[u][e]), zs, -mxs));
+              z[u][e] = __float_as_uint(ex);
+              sum += ex;
+              sdp = fmaf(ex, __uint_as_float(d[u][e]), sdp);
+            }
+          }
+      }
+      red[(kParts + part) * 128 + r] = sum;
+      red[(2 * kParts + part) * 128 + r] = sdp;
+      named_sync(1, kParts * 128);
+      sum = 0.f;
+      sdp = 0.f;
+#pragma unroll
+      for (int u = 0; u < kParts; ++u) {
+        sum += red[(kParts + u) * 128 + r];
+        sdp += red[(2 * kParts + u) * 128 + r];
+      }
+      const float lse2 = mxs + __log2f(sum);
+      const float Dv = p.alpha * sdp / sum;
+      const float pscale = valid ? 1.f / sum : 0.f;
+      if (ok) {
+#pragma unroll
+        for (int u = 0; u < kMine; ++u) {
+          const int s = part + u * kParts;
+          if (s == 7) {
+            // transposed meta tiles: row m, column r
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float pe = __uint_as_float(z[u][e]) * pscale;
+              const float de = pe * fmaf(p.alpha, __uint_as_float(d[u][e]), -Dv);
+              *reinterpret_cast<bf16*>(sm + QS_DSM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(de);
+              *reinterpret_cast<bf16*>(sm + QS_PM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(pe);
+            }
+          } else if (slot_used(s)) {
+            // ds in two 8-column halves (one 16-byte store each)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int e0 = 8 * hf + 2 * e;
+                const float p0 = __uint_as_float(z[u][e0]) * pscale;
+                const float p1 = __uint_as_float(z[u][e0 + 1]) * pscale;
+                w[e] = pack_bf16x2(p0 * fmaf(p.alpha, __uint_as_float(d[u][e0]), -Dv),
+                                   p1 * fmaf(p.alpha, __uint_as_float(d[u][e0 + 1]), -Dv));
+              }
+              *reinterpret_cast<uint4*>(dsb + sw128_offset(r, 16 * (g_lo + s) + 8 * hf, kB)) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+      // band groups no row of this quadrant sees hold zeros (the tile still holds V)
+      for (int g = part; g < kBand / 16; g += kParts)
+        if (g < g_lo || g > g_hi) zero16_bf16(dsb, kB, r, 16 * g);
+      if (M == 0 && part == kParts - 1) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          *reinterpret_cast<bf16*>(sm + QS_DSM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(0.f);
+          *reinterpret_cast<bf16*>(sm + QS_PM + sw128_offset(e, r, kMetaRows)) = __float2bfloat16_rn(0.f);
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(&ctl->bar[Q_DS]);
+      if (ok && valid && part == 0) {
+        p.lse2[(size_t)bh * L + i] = lse2;
+        p.Dw[(size_t)bh * L + i] = Dv;
+      }
+      // dQ out of TMEM into the staging tile: this warp takes the 16-column slices
+      // c = 16 part, 16 (part + kParts), ...; the last warp of the quadrant also the meta
+      // products.  Then the next block's Z may overwrite these columns.
+      const bool meta_here = M > 0 && part == kParts - 1;
+      if (ok && (ok = wait_bar(ctl, Q_OUT, k & 1))) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 16 * part; c < kD; c += 16 * kParts) {
+          uint32_t v[16];
+          tmem_ld16(tl + TQ_DQ + c, v);
+          tmem_ld_wait();
           float w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = p.scale * __uint_as_float(v[16 * h + e]);
-          store16_bf16(sm + QS_Q, kB, r, c + 16 * h, w);
+          for (int e = 0; e < 16; ++e) w[e] = p.scale * __uint_as_float(v[e]);
+          store16_bf16(sm + QS_DQS, kB, r, c, w);
         }
-      }
-      fence_proxy_async_smem();
-      if (M > 0) {
-        // lane r of the meta products = feature dimension r
-        uint32_t mk[16], mv[16];
-        tmem_ld16(tl + TQ_MK, mk);
-        tmem_ld16(tl + TQ_MV, mv);
-        tmem_ld_wait();
-        float* part = p.mpart + ((size_t)bh * p.nq + qb) * M * 256;
+        fence_proxy_async_smem();
+        if (meta_here) {
+          // lane r of the meta products = feature dimension r
+          float* mp = p.mpart + ((size_t)bh * p.nq + qb) * M * 256 + r;
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            uint32_t mk[16];
+            tmem_ld16(tl + (h ? TQ_MV : TQ_MK), mk);
+            tmem_ld_wait();
 #pragma unroll
-        for (int m = 0; m < kMetaRows; ++m) {
-          if (m < M) {
-            part[m * 256 + r] = __uint_as_float(mk[m]);
-            part[m * 256 + 128 + r] = __uint_as_float(mv[m]);
+            for (int m = 0; m < kMetaRows; ++m)
+              if (m < M) mp[m * 256 + 128 * h] = __uint_as_float(mk[m]);
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(&ctl->bar[Q_TMF]);
+      named_sync(1, kParts * 128);
+      if (ok && threadIdx.x == 64) {
+        // rows at or beyond L are clipped by the store
+        tma_store_3d(&maps.dqo, sm + QS_DQS, 0, i0, bh);
+        tma_store_3d(&maps.dqo, sm + QS_DQS + 16384, 64, i0, bh);
+        bulk_commit();
+      }
     }
-    named_sync(1, 128);
-    if (ok && threadIdx.x == 64) {
-      // rows at or beyond L are clipped by the store
-      tma_store_3d(&maps.dqo, sm + QS_Q, 0, i0, bh);
-      tma_store_3d(&maps.dqo, sm + QS_Q + 16384, 64, i0, bh);
-      bulk_commit();
-      bulk_wait_read();
-    }
+    if (threadIdx.x == 64) bulk_wait_read();
     if (!ok) ctl->abort = 1;
   }
 
@@ -357,7 +415,14 @@ win_q_kernel(const __grid_constant__ QMaps maps, const Params p) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if (threadIdx.x == 0 && ctl->abort) raise_status(p.status, kDevTimeout);
+  if (threadIdx.x == 0) {
+    if (ctl->abort) raise_status(p.status, kDevTimeout);
+    // every CTA has taken its last block index once all have come here
+    if (atomicAdd(p.tiles + 1, 1u) == gridDim.x - 1) {
+      p.tiles[0] = 0;
+      p.tiles[1] = 0;
+    }
+  }
 }
 
 // ------------------------------------------------------------------------------------
@@ -391,7 +456,7 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
   float* rd = rl + kBand;                             // D of the band's query rows
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i <= K_DONE; ++i) mbar_init(&ctl->bar[i], i == K_PDS ? 128u : 1u);
+    for (int i = 0; i <= K_DONE; ++i) mbar_init(&ctl->bar[i], i == K_PDS ? kParts * 128u : 1u);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -472,19 +537,20 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
       drain_bar(ctl, K_DONE, 1, globaltimer_ns());
     }
   } else {
+    // kParts warps share each 32-lane TMEM quadrant (as in the query kernel)
     const int qw = warp & 3;
+    const int part = (warp - 2) >> 2;
     const int jr = qw * 32 + lane;  // key row of the block
     const int j = j0 + jr;
     const bool valid = j < L;
     const uint32_t tl = tmem + ((uint32_t)(qw * 32) << 16);
     const float zs = p.scale * kLog2e;
-    const int et = threadIdx.x - 64;  // 0..127
-    for (int u = et; u < kBand; u += 128) {
+    for (int u = threadIdx.x - 64; u < kBand; u += kParts * 128) {
       const int i = j0 + u;
       rl[u] = i < L ? p.lse2[(size_t)bh * L + i] : INFINITY;
       rd[u] = i < L ? p.Dw[(size_t)bh * L + i] : 0.f;
     }
-    named_sync(1, 128);
+    named_sync(1, kParts * 128);
     // query column u <-> query i = j0 + u; this row is seen by u in [jr, jr + W - 1]
     const int g_lo = (32 * qw) >> 4;
     const int g_hi = min(kBand - 1, 32 * qw + 31 + W - 1) >> 4;
@@ -493,22 +559,22 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
     bool ok = wait_bar(ctl, K_SF, 0);
     if (ok) {
       tc_fence_after();
-      // at most six 16-column groups (W <= 65); the next group's TMEM loads are in flight
-      // while this one is worked on
-      constexpr int kNG = 7;
+      // at most six 16-column groups (W <= 65); this warp takes groups g_lo + part,
+      // g_lo + part + kParts, ... and reads them from TMEM with one wait
+      constexpr int kMine = (6 + kParts - 1) / kParts;
       const int ng = g_hi - g_lo + 1;
-      uint32_t sv[2][16], dv[2][16];
-      tmem_ld16(tl + TK_S + 16 * g_lo, sv[0]);
-      tmem_ld16(tl + TK_DP + 16 * g_lo, dv[0]);
+      uint32_t sv[kMine][16], dv[kMine][16];
+#pragma unroll
+      for (int u = 0; u < kMine; ++u)
+        if (part + u * kParts < ng) {
+          tmem_ld16(tl + TK_S + 16 * (g_lo + part + u * kParts), sv[u]);
+          tmem_ld16(tl + TK_DP + 16 * (g_lo + part + u * kParts), dv[u]);
+        }
       tmem_ld_wait();
 #pragma unroll
-      for (int k = 0; k < kNG; ++k) {
-        if (k < ng) {
-          const int g = g_lo + k;
-          if (k + 1 < ng) {
-            tmem_ld16(tl + TK_S + 16 * (g + 1), sv[(k + 1) & 1]);
-            tmem_ld16(tl + TK_DP + 16 * (g + 1), dv[(k + 1) & 1]);
-          }
+      for (int u = 0; u < kMine; ++u) {
+        if (part + u * kParts < ng) {
+          const int g = g_lo + part + u * kParts;
           // columns of the group that see this key: bits lo .. hi
           const int lo = max(jr - 16 * g, 0), hi = min(jr + W - 1 - 16 * g, 15);
           const uint32_t mk = (!valid || hi < lo) ? 0u : ((0xffffu >> (15 - hi)) >> lo) << lo;
@@ -523,17 +589,16 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
           float pp[16], ds[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float pe = (mk & (1u << e)) ? ex2_approx(fmaf(__uint_as_float(sv[k & 1][e]), zs, -rlv[e])) : 0.f;
+            const float pe = (mk & (1u << e)) ? ex2_approx(fmaf(__uint_as_float(sv[u][e]), zs, -rlv[e])) : 0.f;
             pp[e] = pe;
-            ds[e] = pe * fmaf(p.alpha, __uint_as_float(dv[k & 1][e]), -rdv[e]);
+            ds[e] = pe * fmaf(p.alpha, __uint_as_float(dv[u][e]), -rdv[e]);
           }
           store16_bf16(pt, kB, jr, 16 * g, pp);
           store16_bf16(dst, kB, jr, 16 * g, ds);
-          tmem_ld_wait();
         }
       }
     }
-    for (int g = 0; g < kBand / 16; ++g) {
+    for (int g = part; g < kBand / 16; g += kParts) {
       if (g < g_lo || g > g_hi) {
         zero16_bf16(pt, kB, jr, 16 * g);
         zero16_bf16(dst, kB, jr, 16 * g);
@@ -545,8 +610,9 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
     const bool ready = ok && (ok = wait_bar(ctl, K_OUT, 0)) && (ok = wait_bar(ctl, K_DVA, 0));
     if (ready) {
       tc_fence_after();
+      // this warp takes the 32-column slices c = 32 part, 32 (part + kParts), ...
 #pragma unroll 1
-      for (int c = 0; c < kD; c += 32) {
+      for (int c = 32 * part; c < kD; c += 32 * kParts) {
         uint32_t v[32], k[32];
         tmem_ld32(tl + TK_DV + c, v);
         tmem_ld32(tl + TK_DK + c, k);
@@ -572,7 +638,7 @@ win_k_kernel(const __grid_constant__ KMaps maps, const Params p) {
       }
       fence_proxy_async_smem();
     }
-    named_sync(1, 128);
+    named_sync(1, kParts * 128);
     if (ready && threadIdx.x == 64) {
       // rows at or beyond L are clipped by the stores
       tma_store_3d(&maps.dvo, sm + KS_DVS, 0, j0, bh);
@@ -669,7 +735,9 @@ static cudaError_t launch_win_part(int part, const BwdArgs& a, const float* dvac
   p.M = a.M;
   p.W = a.W;
   p.nq = nq;
+  p.nbh = BH;
   p.ahead = ctas_per_wave(1);
+  p.tiles = a.status + kWsWinTiles;
   p.scale = a.scale;
   p.alpha = a.alpha;
   p.lse2 = lse2;
@@ -682,7 +750,8 @@ static cudaError_t launch_win_part(int part, const BwdArgs& a, const float* dvac
   p.status = a.status;
   const int grid = BH * nq;
   cudaError_t e = part == 1 ? launch_tc(win_k_kernel, km, p, grid, kKSmem, "win_bwd_k_tc", s)
-                            : launch_tc(win_q_kernel, qm, p, grid, kQSmem, "win_bwd_q_tc", s);
+                            : launch_tc(win_q_kernel, qm, p, std::min(grid, ctas_per_wave(1)), kQSmem,
+                                        "win_bwd_q_tc", s);
   ++*launches;
   return e;
 }

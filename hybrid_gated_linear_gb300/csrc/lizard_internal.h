@@ -22,6 +22,10 @@ enum : unsigned { kDevTimeout = 1u, kDevCheck = 2u };
 constexpr size_t kWsHeader = 256;
 // Word of the header that counts the tensor-core path's wide chunks (zeroed per call).
 constexpr int kWsWideCount = 4;
+// Words of the header that hand out the window-backward query blocks: the block counter
+// and the count of CTAs done; zero at every call (the header is cleared) and left at zero
+// by every launch that completes.
+constexpr int kWsWinTiles = 8;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
