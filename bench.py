@@ -65,22 +65,28 @@ ALGO_BYTES_PER_TOKEN_HEAD = {
 # (its summary is kept under profiles/), each with the sha256 of the kernel source it was
 # taken on: a kernel whose source changed since then reports "traffic": null.
 PROFILED_TRAFFIC = {
-    "fwd_prep": {"bytes_per_token_head": 1455, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
-               "sha256": "2c9e1070d71be0a0efe6535b2264d9e75664ab6847f4766b7ca3fc3b780ccd0c"},
-    "fwd_scan_tc": {"bytes_per_token_head": 541, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
-                  "sha256": "2c9e1070d71be0a0efe6535b2264d9e75664ab6847f4766b7ca3fc3b780ccd0c"},
-    "fwd_chunk_tc": {"bytes_per_token_head": 1703, "source": "hybrid_gated_linear_gb300/csrc/k_fwd_chunk_tc.cu",
-                   "sha256": "632e7a89c2eb4b97d1e0c0ccaf49ea068a76f68e7ab3209b85a4e543df883d60"},
+    "fwd_prep": {"bytes_per_token_head": 1457, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
+                "sha256": "68fe1a6b61374f3ff34b4103e79112b71830ba2c3ce1b7359618647e046a8649"},
+    "fwd_scan_tc": {"bytes_per_token_head": 546, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
+                   "sha256": "68fe1a6b61374f3ff34b4103e79112b71830ba2c3ce1b7359618647e046a8649"},
+    "fwd_chunk_tc": {"bytes_per_token_head": 1706, "source": "hybrid_gated_linear_gb300/csrc/k_fwd_chunk_tc.cu",
+                    "sha256": "678ea4669c9ac1d5ebd2e018839c5fb78b2859400ed783fd9c7da0afb7f24b4e"},
+    "fwd_wide_fix": {"bytes_per_token_head": 0, "source": "hybrid_gated_linear_gb300/csrc/k_fwd_simt.cu",
+                    "sha256": "45c9f0691c0b9e76e0bf796f61f3d58060713e7470a6126e5fd42e03627e4856"},
+    "win_bwd_q_tc": {"bytes_per_token_head": 1174, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
+                    "sha256": "399849df8ea71bf9b262df7747e75e47c5be1186793612f1f8462683a766a560"},
     "bwd_scan_tc": {"bytes_per_token_head": 541, "source": "hybrid_gated_linear_gb300/csrc/k_gla_states_tc.cu",
-                  "sha256": "2c9e1070d71be0a0efe6535b2264d9e75664ab6847f4766b7ca3fc3b780ccd0c"},
-    "bwd_chunk_tc": {"bytes_per_token_head": 3052, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
-                   "sha256": "cffaffb1a8cad5556498febfe864e690d133a844031754264c8b140febbee8fc"},
-    "bwd_suffix": {"bytes_per_token_head": 549, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
-                 "sha256": "cffaffb1a8cad5556498febfe864e690d133a844031754264c8b140febbee8fc"},
-    "win_bwd_q_tc": {"bytes_per_token_head": 1170, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
-                   "sha256": "7ec0ebd48d5bb82652fc88fdc08b4afe070194fe483214165237362664fd14bb"},
-    "win_bwd_k_tc": {"bytes_per_token_head": 1884, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
-                   "sha256": "7ec0ebd48d5bb82652fc88fdc08b4afe070194fe483214165237362664fd14bb"},
+                   "sha256": "68fe1a6b61374f3ff34b4103e79112b71830ba2c3ce1b7359618647e046a8649"},
+    "bwd_chunk_tc": {"bytes_per_token_head": 3037, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
+                    "sha256": "744fd77ad071cfd9b6fb2830eac33ad4a3c734419ef304aca9475664563ec048"},
+    "bwd_wide_fix": {"bytes_per_token_head": 0, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_simt.cu",
+                    "sha256": "eb001aa4f6f4afd3013c8db745462b31f6eb4870b4e1d1fc2824f8267b37c7d6"},
+    "bwd_suffix": {"bytes_per_token_head": 553, "source": "hybrid_gated_linear_gb300/csrc/k_bwd_tc.cu",
+                  "sha256": "744fd77ad071cfd9b6fb2830eac33ad4a3c734419ef304aca9475664563ec048"},
+    "win_bwd_k_tc": {"bytes_per_token_head": 1891, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
+                    "sha256": "399849df8ea71bf9b262df7747e75e47c5be1186793612f1f8462683a766a560"},
+    "win_bwd_meta": {"bytes_per_token_head": 32, "source": "hybrid_gated_linear_gb300/csrc/k_win_bwd_tc.cu",
+                    "sha256": "399849df8ea71bf9b262df7747e75e47c5be1186793612f1f8462683a766a560"},
 }
 
 DECODE_BYTES_PER_UNIT = 2 * 65536 + 2 * 64 * 128 * 2 + 5 * 256 + 512 + 2 * 256 + 256
@@ -481,6 +487,42 @@ def _decode_part(dev, stream, peaks, steps=64):
                          "algorithmic_bytes_per_step": DECODE_BYTES_PER_UNIT * units}}
 
 
+def _std_gla_part(dev, flush, prob, clocks_mhz=None, reps=10):
+    """The standard fp32 chunkwise GLA forward (lizard_gla_std_fwd: CUDA-core FFMA, GLA branch
+    only) against lizard_attn_fwd (bf16 tensor cores, GLA and window branches) on the same
+    inputs, L2 flushed before each launch.  The pages' comparison ("Lizard", Efficiency,
+    Table 3) is forward latency of the Lizard kernel against a standard GLA forward."""
+    import torch
+
+    import hybrid_gated_linear_gb300 as lz
+    t, w = prob.t, prob.w
+    dims = prob.dims
+    ws = torch.zeros(lz.lizard_gla_std_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+    y = torch.empty_like(prob.y)
+    std = lambda: lz.lizard_gla_std_fwd(dims, t["phi_q"], t["phi_k"], t["v"], t["log_gamma"], y,
+                                        None, None, ws)
+    for _ in range(3):
+        std()
+        prob.fwd()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    std_ms = statistics.median(_time_steps(std, reps, flush, stream))
+    liz_ms = statistics.median(_time_steps(prob.fwd, reps, flush, stream))
+    status = lz.lizard_check_device_errors(ws)
+    # useful multiply-adds per 64-token chunk: chunk state 64 D^2, causal Qt Kt^T and S V
+    # 64^2 D / 2 each, Qt h 64 D^2; two flops each
+    D, units = w["dk"], w["B"] * w["H"] * w["L"]
+    flops = 2.0 * (2 * 64 * D * D + 64 * 64 * D) * units / 64
+    return {"workload": f"GLA forward B={w['B']}, H={w['H']}, L={w['L']}, d={D}, bf16 inputs; "
+                        "L2 flushed before each launch",
+            "standard_gla_fp32_ms": std_ms, "lizard_attn_fwd_ms": liz_ms,
+            "lizard_speedup": std_ms / liz_ms,
+            "standard_gla_tflops": flops / (std_ms * 1e-3) / 1e12,
+            "standard_gla_status": status,
+            "note": "lizard_attn_fwd also computes the window branch; the standard kernel "
+                    "computes the GLA branch only"}
+
+
 def _fmap_part(dev, peaks, flush, prob, reps=20):
     """Hedgehog feature map on the attention workload's shape (B=1, H=32, L=4096, D=128
     input features, F=64, bf16): forward and backward timed separately with CUDA events,
@@ -786,6 +828,11 @@ def run_ours(args):
             parts["decode"] = _decode_part(dev, stream, peaks)
         except Exception as e:  # reported, never hidden
             parts["decode"] = {"error": repr(e)}
+    if "stdgla" in want:
+        try:
+            parts["standard_gla"] = _std_gla_part(dev, flush, prob)
+        except Exception as e:  # reported, never hidden
+            parts["standard_gla"] = {"error": repr(e)}
     if "fmap" in want:
         try:
             parts["feature_map"] = _fmap_part(dev, peaks, flush, prob)
@@ -856,9 +903,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-train-part", action="store_true",
                     help="skip the training-workload line in parts (a shorter run)")
-    ap.add_argument("--parts", default="decode,fmap,long,train",
+    ap.add_argument("--parts", default="decode,fmap,long,train,stdgla",
                     help="comma list of the extra sections measured after the step: decode, "
-                         "fmap, long (long context), train (the B=8 L=2048 step); '' for none")
+                         "fmap, long (long context), train (the B=8 L=2048 step), stdgla (the "
+                         "standard fp32 GLA forward against ours); '' for none")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

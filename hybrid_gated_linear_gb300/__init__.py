@@ -27,8 +27,8 @@ __all__ = [
     "lizard_decode_ring_fill", "lizard_state_combine", "lizard_fmap_dims",
     "lizard_feature_map_fwd", "lizard_feature_map_bwd", "lizard_feature_map_workspace_bytes",
     "lizard_attn_fwd_fmap", "lizard_selftest_wait_timeout", "lizard_gate_dims",
-    "lizard_gate_fwd", "lizard_gate_bwd", "lizard_gate_workspace_bytes", "LIZARD_F32",
-    "LIZARD_BF16", "EXPORTED_SYMBOLS",
+    "lizard_gate_fwd", "lizard_gate_bwd", "lizard_gate_workspace_bytes", "lizard_gla_std_fwd",
+    "lizard_gla_std_workspace_bytes", "LIZARD_F32", "LIZARD_BF16", "EXPORTED_SYMBOLS",
 ]
 
 LIZARD_F32 = 0
@@ -44,7 +44,7 @@ EXPORTED_SYMBOLS = (
     "lizard_decode_ring_fill", "lizard_state_combine", "lizard_feature_map_fwd",
     "lizard_feature_map_bwd", "lizard_feature_map_workspace_bytes", "lizard_attn_fwd_fmap",
     "lizard_selftest_wait_timeout", "lizard_gate_fwd", "lizard_gate_bwd",
-    "lizard_gate_workspace_bytes",
+    "lizard_gate_workspace_bytes", "lizard_gla_std_fwd", "lizard_gla_std_workspace_bytes",
 )
 
 STATUS_NAMES = {0: "LIZARD_OK", 1: "LIZARD_ERR_INVALID_ARG", 2: "LIZARD_ERR_UNSUPPORTED",
@@ -132,6 +132,8 @@ def library():
                 "lizard_gate_workspace_bytes": (SZ, [GDP]),
                 "lizard_gate_fwd": (I32, [GDP, P, P, P, P]),
                 "lizard_gate_bwd": (I32, [GDP, P, P, P, P, P, P, SZ, P]),
+                "lizard_gla_std_workspace_bytes": (SZ, [DP]),
+                "lizard_gla_std_fwd": (I32, [DP] + [P] * 8 + [SZ, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -255,6 +257,19 @@ def lizard_attn_fwd(dims: lizard_dims, phi_q, phi_k, v, log_gamma, q, k, meta_k,
                                    int(W), float(alpha), _ptr(y), _ptr(h0), _ptr(h_final),
                                    _ptr(workspace), _ws_bytes(workspace), _stream(stream))
     _check(st, "lizard_attn_fwd")
+
+
+def lizard_gla_std_workspace_bytes(dims: lizard_dims) -> int:
+    return library().lizard_gla_std_workspace_bytes(ctypes.byref(dims))
+
+
+def lizard_gla_std_fwd(dims: lizard_dims, phi_q, phi_k, v, log_gamma, y, h0, h_final, workspace,
+                       stream=None):
+    """The standard fp32 chunkwise GLA forward (GLA branch only) into preallocated ``y``."""
+    st = library().lizard_gla_std_fwd(ctypes.byref(dims), _ptr(phi_q), _ptr(phi_k), _ptr(v),
+                                      _ptr(log_gamma), _ptr(y), _ptr(h0), _ptr(h_final),
+                                      _ptr(workspace), _ws_bytes(workspace), _stream(stream))
+    _check(st, "lizard_gla_std_fwd")
 
 
 def lizard_attn_bwd(dims: lizard_dims, phi_q, phi_k, v, log_gamma, q, k, meta_k, meta_v, W: int,

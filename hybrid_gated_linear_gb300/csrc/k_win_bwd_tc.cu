@@ -672,7 +672,16 @@ __global__ void __launch_bounds__(256) win_meta_kernel(int B, int H, int M, int 
   float s = 0.f;
   for (int b = 0; b < B; ++b) {
     const float* part = mpart + ((size_t)(b * H + hh) * nq) * M * 256 + m * 256 + d;
-    for (int q = 0; q < nq; ++q) s += part[(size_t)q * M * 256];
+    // eight loads in flight, added in block order
+    int q = 0;
+    for (; q + 8 <= nq; q += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = part[(size_t)(q + u) * M * 256];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) s += v[u];
+    }
+    for (; q < nq; ++q) s += part[(size_t)q * M * 256];
   }
   if (d < kD) dmk[((size_t)hh * M + m) * kD + d] = scale * s;
   else dmv[((size_t)hh * M + m) * kD + d - kD] = alpha * s;

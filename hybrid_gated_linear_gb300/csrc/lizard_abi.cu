@@ -656,6 +656,48 @@ lizard_status lizard_gate_bwd(const lizard_gate_dims* dims, const void* x, const
   return cuda_status(e);
 }
 
+size_t lizard_gla_std_workspace_bytes(const lizard_dims* dims) {
+  if (!dims_ok(dims) || shape_supported(dims->dk, dims->dv) != LIZARD_OK) return 0;
+  return lz::kWsHeader + lz::gla_std_workspace(dims->B * dims->H, dims->L, dims->dk);
+}
+
+lizard_status lizard_gla_std_fwd(const lizard_dims* dims, const void* phi_q, const void* phi_k,
+                                 const void* v, const float* log_gamma, void* y, const float* h0,
+                                 float* h_final, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  g_last_launches = 0;
+  if (!dims_ok(dims)) return LIZARD_ERR_INVALID_ARG;
+  const lizard_dims& d = *dims;
+  const bool tok = d.L > 0;
+  if (!ptr_ok(phi_q, !tok) || !ptr_ok(phi_k, !tok) || !ptr_ok(v, !tok) ||
+      !ptr_ok(log_gamma, !tok) || !ptr_ok(y, !tok) || !ptr_ok(h0, true) || !ptr_ok(h_final, true))
+    return LIZARD_ERR_INVALID_ARG;
+  lizard_status st = shape_supported(d.dk, d.dv);
+  if (st != LIZARD_OK) return st;
+  if ((long long)d.B * d.H > 65535LL) return LIZARD_ERR_UNSUPPORTED;
+  const size_t need = lizard_gla_std_workspace_bytes(dims);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return LIZARD_ERR_WORKSPACE;
+  const size_t es = elem_size(d.dtype);
+  const size_t ny = (size_t)d.B * d.H * d.L * d.dv * es;
+  const size_t nk = (size_t)d.B * d.H * d.L * d.dk * es;
+  const size_t nh = (size_t)d.B * d.H * d.dk * d.dv * sizeof(float);
+  struct Span { const void* p; size_t n; };
+  const Span ins[] = {{phi_q, nk}, {phi_k, nk}, {v, ny}, {log_gamma, nk / es * 4}, {h0, nh},
+                      {workspace, workspace_bytes}};
+  for (const Span& in : ins)
+    if (overlap(y, ny, in.p, in.n) || overlap(h_final, nh, in.p, in.n)) return LIZARD_ERR_INVALID_ARG;
+  if (overlap(y, ny, h_final, nh)) return LIZARD_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemsetAsync(workspace, 0, lz::kWsHeader, s) != cudaSuccess) return LIZARD_ERR_CUDA;
+  int launches = 0;
+  const cudaError_t e = lz::launch_gla_std_fwd(
+      d.B * d.H, d.L, d.dk, d.dtype, phi_q, phi_k, v, log_gamma, h0, h_final, y,
+      static_cast<unsigned*>(workspace), static_cast<unsigned char*>(workspace) + lz::kWsHeader, s,
+      &launches);
+  g_last_launches = launches;
+  return cuda_status(e);
+}
+
 size_t lizard_fwd_bwd_host_workspace_bytes(const lizard_dims* dims, int32_t W) {
   if (!dims_ok(dims) || W < 1 || shape_supported(dims->dk, dims->dv) != LIZARD_OK) return 0;
   const int Hs = host_slice_heads(dims->H);

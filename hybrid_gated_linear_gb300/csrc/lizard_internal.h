@@ -268,6 +268,14 @@ cudaError_t launch_fmap_bwd(int B, int H, int L, int D, int F, lizard_dtype dt, 
 
 // Gate projection log gamma = logsigmoid(x W) / tau and its backward (k_gate.cu).
 size_t gate_bwd_workspace(int B, int H, int L, int D, int dk);
+// The standard (fp32, CUDA-core) chunkwise GLA forward used as the comparison point
+// (k_gla_std.cu).
+size_t gla_std_workspace(int BH, int L, int D);
+cudaError_t launch_gla_std_fwd(int BH, int L, int D, lizard_dtype dt, const void* pq,
+                               const void* pk, const void* v, const float* lg, const float* h0,
+                               float* hf, void* y, unsigned* status, unsigned char* ws,
+                               cudaStream_t s, int* launches);
+
 cudaError_t launch_gate_fwd(int B, int H, int L, int D, int dk, lizard_dtype dt, float tau,
                             const void* x, const void* w, float* lg, cudaStream_t s, int* launches);
 cudaError_t launch_gate_bwd(int B, int H, int L, int D, int dk, lizard_dtype dt, float tau,

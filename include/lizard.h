@@ -349,6 +349,32 @@ lizard_status lizard_gate_bwd(const lizard_gate_dims* dims, const void* x, const
                               size_t workspace_bytes, void* stream);
 
 /*
+ * The "standard" chunkwise GLA forward, the comparison point of the hardware-aware kernel
+ * (not part of the Lizard operator).  "Lizard" (arXiv 2507.09025), Preliminaries: the
+ * matrix form of GLA needs the cumulative gate products in full precision, so standard
+ * GLA kernels fall back to fp32 arithmetic without tensor cores; Efficiency, Table 3:
+ * forward latency of the Lizard kernel against such a standard GLA.  This call computes
+ * the GLA branch alone,
+ *   y_i = phi_q_i^T h_i,  h_i = gamma_i (.) h_{i-1} + phi_k_i v_i^T  (h_{-1} = h0),
+ * chunkwise over 64-token chunks with every operand and product in fp32 on CUDA cores
+ * (FFMA): chunk states K^T V, a scan over chunks, then tril(Qt Kt^T) V + Qt h per chunk
+ * with Qt = phi_q e^{b}, Kt = phi_k e^{-b} (b the chunk-local cumulative log gate).
+ *   dims: B, H, L, dk = dv in {64, 128}, dtype (M and scale are ignored); B * H <= 65535.
+ *   phi_q, phi_k [B,H,L,dk] T;  v [B,H,L,dv] T;  log_gamma [B,H,L,dk] fp32;  y [B,H,L,dv] T
+ *   output;  h0, h_final [B,H,dk,dv] fp32 or NULL.
+ *   workspace: lizard_gla_std_workspace_bytes(dims) bytes (every chunk's state in fp32),
+ *   caller-owned, 16-byte aligned.
+ * The factorised form has no finite value when the cumulative log gate inside a chunk
+ * leaves [-80, 80]; such a chunk sets LIZARD_ERR_DEVICE_CHECK in the workspace status word
+ * (lizard_attn_fwd has no such limit).
+ */
+size_t lizard_gla_std_workspace_bytes(const lizard_dims* dims);
+lizard_status lizard_gla_std_fwd(const lizard_dims* dims, const void* phi_q, const void* phi_k,
+                                 const void* v, const float* log_gamma, void* y, const float* h0,
+                                 float* h_final, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/*
  * Self-test of the device-side failure detection (a library service; the pages have no
  * counterpart).  Every wait of the tile kernels on an mbarrier is bounded: when it runs
  * out the CTA stops its other roles, drains what it has in flight, frees its tensor
