@@ -7,7 +7,31 @@
 
 #include <mutex>
 
+#include "lizard_dev.cuh"
 #include "lizard_internal.h"
+
+namespace {
+
+// Clears the workspace header (status word and counters) in stream order.  A one-CTA
+// kernel launched as a programmatic dependent: it waits for the previous kernel on the
+// stream like a memset would, but its launch overlaps that kernel's tail and the next
+// kernel can be launched before it ends, which a memset node prevents.
+__global__ void header_reset_kernel(unsigned* w) {
+  lz::pdl_wait();
+  for (int i = threadIdx.x; i < (int)(lz::kWsHeader / sizeof(unsigned)); i += blockDim.x) w[i] = 0u;
+  lz::pdl_trigger();
+}
+
+cudaError_t reset_header(void* workspace, cudaStream_t s, int* launches) {
+  lz::trace_begin("header_reset", s);
+  const cudaError_t e = lz::launch_pdl(header_reset_kernel, dim3(1), dim3(64), 0, s,
+                                       static_cast<unsigned*>(workspace));
+  lz::trace_end(s);
+  ++*launches;
+  return e;
+}
+
+}  // namespace
 
 namespace {
 
@@ -282,7 +306,8 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* phi_q, const 
     return LIZARD_ERR_INVALID_ARG;
 
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = cudaMemsetAsync(workspace, 0, lz::kWsHeader, s);
+  int launches = 0;
+  cudaError_t e = reset_header(workspace, s, &launches);
   if (e != cudaSuccess) return LIZARD_ERR_CUDA;
   // A window longer than the sequence sees the same keys as one of length L.
   const int W_eff = d.L > 0 && W > d.L ? d.L : W;
@@ -290,7 +315,6 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* phi_q, const 
                 phi_q, phi_k, v, log_gamma, q, k, meta_k, meta_v, y, h0, h_final,
                 static_cast<unsigned*>(workspace),
                 static_cast<unsigned char*>(workspace) + lz::kWsHeader};
-  int launches = 0;
   e = dispatch_fwd(a, d.dtype, s, &launches);
   g_last_launches = launches;
   return cuda_status(e);
@@ -400,10 +424,11 @@ lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* phi_q, const 
       if (overlap(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return LIZARD_ERR_INVALID_ARG;
   }
 
-  cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = cudaMemsetAsync(workspace, 0, lz::kWsHeader, s);
-  if (e != cudaSuccess) return LIZARD_ERR_CUDA;
   if (W_eff > kMaxBwdWindow) return LIZARD_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  int launches = 0;
+  cudaError_t e = reset_header(workspace, s, &launches);
+  if (e != cudaSuccess) return LIZARD_ERR_CUDA;
   lz::BwdArgs a{d.B, d.H, d.L, d.dk, d.dv, d.M, W_eff, resolve_scale(d.scale, d.dk), alpha,
                 phi_q, phi_k, v, log_gamma, q, k, meta_k, meta_v, h0, dy,
                 d_phi_q, d_phi_k, d_v, d_log_gamma, d_q, d_k, d_meta_k, d_meta_v, d_h0,
@@ -413,7 +438,6 @@ lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* phi_q, const 
                 fwd_workspace ? static_cast<unsigned char*>(const_cast<void*>(fwd_workspace)) +
                                     lz::kWsHeader
                               : nullptr};
-  int launches = 0;
   e = lz::launch_bwd_simt(a, d.dtype, s, &launches);
   g_last_launches = launches;
   return cuda_status(e);
