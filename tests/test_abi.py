@@ -219,3 +219,40 @@ def test_fused_forward_and_phi_free_backward_validation(lib):
                              1.0, None, P(12), dh(0), dh(1), dh(2), dh(3), dh(4), dh(5), dh(6),
                              dh(7), None, None, dh(8), wsb, None)
     assert rc == INVALID
+
+
+def _std(lib, dims, ptrs=None, y=A + 0x30000000, ws=A + 0x40000000, ws_bytes=1 << 30):
+    p = [ctypes.c_void_p(A + i * 0x1000000) for i in range(4)] if ptrs is None else ptrs
+    return lib.lizard_gla_std_fwd(ctypes.byref(dims) if dims is not None else None, *p,
+                                  ctypes.c_void_p(y) if y else None, None, None,
+                                  ctypes.c_void_p(ws) if ws else None, ws_bytes, None)
+
+
+def test_gla_std_workspace_is_every_chunk_state(lib):
+    """One fp32 D x D state and one Gamma row per 64-token chunk, after the 256-byte header
+    (each part rounded up to 256 bytes)."""
+    for B, H, L, d in ((1, 2, 64, 128), (2, 3, 300, 64), (1, 1, 1, 128)):
+        nc = (L + 63) // 64
+        up = lambda x: (x + 255) // 256 * 256
+        want = 256 + up(B * H * nc * d * d * 4) + up(B * H * nc * d * 4)
+        got = lib.lizard_gla_std_workspace_bytes(ctypes.byref(_dims(B=B, H=H, L=L, dk=d, dv=d)))
+        assert got == want, (B, H, L, d)
+    assert lib.lizard_gla_std_workspace_bytes(ctypes.byref(_dims(dk=96, dv=96))) == 0
+    assert lib.lizard_gla_std_workspace_bytes(None) == 0
+
+
+def test_gla_std_rejects_bad_arguments(lib):
+    assert _std(lib, None) == INVALID
+    assert _std(lib, _dims(B=0)) == INVALID
+    assert _std(lib, _dims(dtype=7)) == INVALID
+    assert _std(lib, _dims(dk=96, dv=96)) == UNSUPPORTED
+    assert _std(lib, _dims(dk=128, dv=64)) == UNSUPPORTED
+    assert _std(lib, _dims(B=300, H=300)) == UNSUPPORTED  # B*H above one grid dimension
+    bad = [ctypes.c_void_p(A + i * 0x1000000) for i in range(4)]
+    bad[1] = ctypes.c_void_p(A + 8)  # misaligned phi_k
+    assert _std(lib, _dims(), ptrs=bad) == INVALID
+    assert _std(lib, _dims(), y=None) == INVALID
+    assert _std(lib, _dims(), y=A) == INVALID  # y over phi_q
+    assert _std(lib, _dims(), ws=None, ws_bytes=0) == WORKSPACE
+    need = lib.lizard_gla_std_workspace_bytes(ctypes.byref(_dims()))
+    assert _std(lib, _dims(), ws_bytes=need - 1) == WORKSPACE
