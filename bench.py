@@ -487,7 +487,7 @@ def _decode_part(dev, stream, peaks, steps=64):
                          "algorithmic_bytes_per_step": DECODE_BYTES_PER_UNIT * units}}
 
 
-def _std_gla_part(dev, flush, prob, clocks_mhz=None, reps=10):
+def _std_gla_part(dev, flush, prob, reps=10):
     """The standard fp32 chunkwise GLA forward (lizard_gla_std_fwd: CUDA-core FFMA, GLA branch
     only) against lizard_attn_fwd (bf16 tensor cores, GLA and window branches) on the same
     inputs, L2 flushed before each launch.  The pages' comparison ("Lizard", Efficiency,
